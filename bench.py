@@ -1,0 +1,393 @@
+#!/usr/bin/env python3
+"""Benchmark of the routed MXFP4 MoE block on GB300: one JSON line on stdout.
+
+A step is one whole forward of the block (router, top-k, expert sort and
+gather, gate_up, down, combine) over one batch of S token rows with all
+weights resident in HBM.  The L2 is flushed (a write of twice its size)
+before every step, outside the timed events; each step is bracketed by CUDA
+events on the launch stream.  Under torchrun each rank runs an independent
+replica (the block does not shard on one box); value = all ranks' tokens / the
+slowest rank's time.
+
+--impl reference times the CPU oracle (the only reference there is: the pages
+publish no implementation) on the host cores instead.
+"""
+from __future__ import annotations
+
+import argparse
+import glob
+import hashlib
+import json
+import os
+import re
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import moe_inputs as mi  # noqa: E402
+
+METRIC = "MoE-layer tokens/s at S=8..128 and achieved HBM GB/s vs 8 TB/s roofline"
+DEFAULT_CONFIG = 1
+PEAKS_FILE = os.path.join(ROOT, "MEASURED_PEAKS.json")
+FALLBACK_HBM_GBS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--config", type=int, default=DEFAULT_CONFIG,
+                    help="index into the workload list (0..4); 1 is the headline workload")
+    ap.add_argument("--timing-steps", type=int, default=200,
+                    help="steps of the per-kernel timing pass (roofline)")
+    ap.add_argument("--cpu-seconds", type=float, default=12.0,
+                    help="budget of the CPU-oracle baseline sample")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    return ap.parse_args()
+
+
+# ---------------------------------------------------------------------------
+# distributed plumbing (replicas only)
+# ---------------------------------------------------------------------------
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def dist_init(ws: int, backend: str):
+    if ws <= 1:
+        return None
+    import torch.distributed as dist
+    os.environ.setdefault("MASTER_ADDR", "127.0.0.1")
+    dist.init_process_group(backend=backend)
+    return dist
+
+
+def aggregate(dist, ms_total: float, units: int, device=None) -> tuple[float, int]:
+    """(max over ranks of the timed milliseconds, sum over ranks of the units)."""
+    if dist is None:
+        return ms_total, units
+    import torch
+    t = torch.tensor([ms_total], dtype=torch.float64, device=device)
+    u = torch.tensor([units], dtype=torch.int64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    dist.all_reduce(u, op=dist.ReduceOp.SUM)
+    return float(t.item()), int(u.item())
+
+
+# ---------------------------------------------------------------------------
+# clocks during the timed region
+# ---------------------------------------------------------------------------
+CLOCK_Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+           "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+           "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+
+class ClockSampler:
+    def __init__(self, gpu_index: int, period_ms: int = 50):
+        self.gpu = gpu_index
+        self.period = period_ms
+        self.proc = None
+        self.path = None
+
+    def start(self):
+        try:
+            fd, self.path = tempfile.mkstemp(suffix=".csv")
+            os.close(fd)
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--id={self.gpu}", f"--query-gpu={CLOCK_Q}", "--format=csv,noheader,nounits",
+                 f"-lms={self.period}", "-f", self.path],
+                stdout=subprocess.DEVNULL, stderr=subprocess.DEVNULL)
+        except (OSError, FileNotFoundError):
+            self.proc = None
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        time.sleep(0.1)
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        rows = []
+        try:
+            for line in open(self.path):
+                f = [c.strip() for c in line.split(",")]
+                if len(f) >= 9 and f[1].replace(".", "").isdigit():
+                    rows.append(f)
+        finally:
+            os.unlink(self.path)
+        if not rows:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        sm = [float(r[1]) for r in rows]
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = [n for i, n in enumerate(names) if any(r[5 + i].lower() == "active" for r in rows)]
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": float(rows[0][2]),
+                "reasons": reasons, "samples": len(rows),
+                "power_w_max": max(float(r[3]) for r in rows if r[3].replace(".", "").isdigit())}
+
+
+# ---------------------------------------------------------------------------
+# roofline helpers
+# ---------------------------------------------------------------------------
+def measured_peaks():
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        return float(p["hbm_gbs"]), "measured"
+    return FALLBACK_HBM_GBS, "fallback"
+
+
+def algorithmic_bytes(cfg: mi.MoEConfig, n_touched: int) -> dict:
+    """Per launch: the bytes each kernel must move at least (weights + scales of
+    the touched experts; the router's weight and bias)."""
+    per_w13 = 2 * cfg.I * cfg.d * 17 // 32
+    per_w2 = cfg.d * cfg.I * 17 // 32
+    return {
+        "gateup": n_touched * per_w13,
+        "down": n_touched * per_w2,
+        "router_logits": cfg.E * cfg.d * 2 + cfg.S * cfg.d * 2,
+        "step": n_touched * (per_w13 + per_w2) + cfg.E * cfg.d * 2 + 4 * cfg.E,
+    }
+
+
+def kernel_source_sha(name: str) -> str:
+    h = hashlib.sha256()
+    for p in sorted(glob.glob(os.path.join(ROOT, "mxfp4_mixture_experts_route_gb300", "csrc", "*"))):
+        h.update(open(p, "rb").read())
+    return h.hexdigest()[:12]
+
+
+def profiled_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from a committed ncu summary of this kernel and
+    workload, if the library sources have not changed since it was taken."""
+    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(path):
+        return None
+    txt = open(path).read()
+    m = re.search(r"dram_bytes_per_launch:\s*([0-9.eE+]+)", txt)
+    s = re.search(r"source_sha:\s*([0-9a-f]+)", txt)
+    if not m or not s or s.group(1) != kernel_source_sha(kernel):
+        return None
+    return float(m.group(1))
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing (baseline and the reference arm)
+# ---------------------------------------------------------------------------
+def oracle_tokens_per_s(inp: mi.MoEInputs, budget_s: float, chunk: int):
+    import oracle as O
+    S = inp.cfg.S
+    done, t0, i = 0, time.perf_counter(), 0
+    while True:
+        rows = np.arange(i, min(S, i + chunk))
+        O.moe_forward(inp, rows)
+        done += len(rows)
+        i = (i + chunk) % S
+        el = time.perf_counter() - t0
+        if el >= budget_s:
+            return done / el, done, el
+
+
+def oracle_threads() -> int:
+    return min(8, os.cpu_count() or 1)
+
+
+def run_reference(args, cfg: mi.MoEConfig):
+    ws, rank, _ = dist_env()
+    if rank != 0:
+        return
+    import oracle as O
+    inp = mi.make_inputs(cfg)
+    chunk = 1
+    for _ in range(args.warmup):
+        O.moe_forward(inp, np.arange(chunk))
+    t0 = time.perf_counter()
+    for s in range(args.steps):
+        O.moe_forward(inp, np.array([s % cfg.S]))
+    el = time.perf_counter() - t0
+    tok = args.steps * chunk
+    val = tok / el
+    line = {
+        "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
+        "data": "synthetic", "config": workload_config(cfg, None),
+        "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+                         "sample": f"1 token row a step (token s mod {cfg.S}), numpy fp64 oracle"},
+        "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line), flush=True)
+
+
+def workload_config(cfg: mi.MoEConfig, n_touched):
+    c = {"workload": cfg.name, "S": cfg.S, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+         "post_norm": cfg.post_norm, "zipf": cfg.zipf, "seed": 0,
+         "l2": "flushed before every timed step (write of 2x the L2 size, outside the events)"}
+    if n_touched is not None:
+        c["n_touched"] = n_touched
+    return c
+
+
+# ---------------------------------------------------------------------------
+# our arm
+# ---------------------------------------------------------------------------
+def run_ours(args, cfg: mi.MoEConfig):
+    import torch
+    import mxfp4_mixture_experts_route_gb300 as moe
+
+    ws_n, rank, local = dist_env()
+    torch.cuda.set_device(local)
+    dist = dist_init(ws_n, "nccl")
+    dev = torch.device("cuda", local)
+
+    inp = mi.make_inputs(cfg)
+    shape = moe.MoEShape.of(cfg.S, cfg.d, cfg.E, cfg.k, cfg.I, post_norm=cfg.post_norm,
+                            logit_offset=bool(cfg.zipf), norm_eps=cfg.norm_eps)
+    blk = moe.DeviceWeights(shape, inp.x, inp.w_gate, inp.bias, inp.logit_off, inp.w13, inp.w13s,
+                            inp.w2, inp.w2s, inp.norm_w, device=dev)
+    l2 = torch.cuda.get_device_properties(dev).L2_cache_size
+    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    for _ in range(args.warmup):
+        flush.zero_()
+        blk.forward()
+    moe.check_device_status(blk.ws, "warmup")
+    ids = blk.ids.cpu().numpy()
+    n_touched = int(len(np.unique(ids)))
+
+    # --- timed region -------------------------------------------------------
+    K = args.steps
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
+    clocks = ClockSampler(local)
+    torch.cuda.synchronize(dev)
+    if dist:
+        dist.barrier()
+    clocks.start()
+    time.sleep(0.05)
+    wall0 = time.perf_counter()
+    for i in range(K):
+        flush.zero_()
+        ev[i][0].record(stream)
+        blk.forward()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    wall = time.perf_counter() - wall0
+    if dist:
+        dist.barrier()
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(b) for a, b in ev]
+    moe.check_device_status(blk.ws, "timed steps")
+    ms_total, units = aggregate(dist, sum(step_ms), K * cfg.S, dev)
+    value = units / (ms_total / 1e3)
+
+    # --- per-kernel timing pass (roofline) ----------------------------------
+    T = max(1, args.timing_steps)
+    launches_per_step = None
+    moe.timing_enable(64 * T)
+    for _ in range(T):
+        flush.zero_()
+        blk.forward()
+    torch.cuda.synchronize(dev)
+    recs = moe.timing_collect(64 * T)
+    moe.timing_enable(0)
+    launches_per_step = len(recs) // T
+    per_kernel = {}
+    for name, ms in recs:
+        per_kernel.setdefault(name, []).append(ms)
+    kmean = {k: statistics.fmean(v) for k, v in per_kernel.items()}
+    ktot = sum(sum(v) for v in per_kernel.values())
+    dom = max(kmean, key=lambda k: sum(per_kernel[k]))
+    hbm_peak, peak_src = measured_peaks()
+    alg = algorithmic_bytes(cfg, n_touched)
+    dom_bytes = alg.get(dom)
+    roof = None
+    if dom_bytes is not None:
+        ach = dom_bytes / (kmean[dom] * 1e-3) / 1e9
+        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+                "frac": ach / hbm_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
+                if peak_src == "measured" else "fallback 6.8 TB/s",
+                "traffic": profiled_traffic(dom, cfg.name),
+                "algorithmic_bytes_per_launch": dom_bytes, "mean_launch_ms": kmean[dom],
+                "share_of_step": sum(per_kernel[dom]) / ktot}
+    step_mean_ms = ms_total / K
+    step_gbs = alg["step"] / (statistics.fmean(step_ms) * 1e-3) / 1e9
+
+    # --- end to end through host buffers ------------------------------------
+    xh = torch.as_tensor(inp.x).view(torch.bfloat16).pin_memory()
+    oh = torch.empty((cfg.S, cfg.d), dtype=torch.float32).pin_memory()
+    ih = torch.empty((cfg.S, cfg.k), dtype=torch.int32).pin_memory()
+    wh = torch.empty((cfg.S, cfg.k), dtype=torch.float32).pin_memory()
+    E2 = min(K, 500)
+    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E2)]
+    for i in range(E2):
+        flush.zero_()
+        ev2[i][0].record(stream)
+        moe.forward_host(shape, xh, blk.w_gate, blk.bias, blk.logit_off, blk.w13, blk.w13s, blk.w2,
+                         blk.w2s, blk.norm_w, ih, wh, oh, blk.ws)
+        ev2[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    moe.check_device_status(blk.ws, "e2e steps")
+    e2e_ms, e2e_units = aggregate(dist, sum(a.elapsed_time(b) for a, b in ev2), E2 * cfg.S, dev)
+    e2e = {"value": e2e_units / (e2e_ms / 1e3), "unit": "tokens/s",
+           "h2d_bytes_per_step": cfg.S * cfg.d * 2,
+           "d2h_bytes_per_step": cfg.S * cfg.d * 4 + cfg.S * cfg.k * 8,
+           "steps": E2, "api": "moe_forward_host (pinned host x in, ids/weights/out back)"}
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        tps, ntok, el = oracle_tokens_per_s(inp, args.cpu_seconds, chunk=min(cfg.S, 8))
+        cpu = {"value": tps, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
+               "sample": f"{ntok} token rows of this workload in chunks of {min(cfg.S, 8)}, "
+                         f"{el:.1f} s, numpy fp64 oracle (expert thread pool of {oracle_threads()})"}
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": K,
+            "warmup": args.warmup, "ms_per_step": step_mean_ms, "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
+            "config": workload_config(cfg, n_touched),
+            "achieved_hbm_gbs_step": step_gbs,
+            "roofline": roof,
+            "kernels_ms": kmean,
+            "cpu_baseline": cpu,
+            "e2e": e2e,
+            "gpu_launches": launches_per_step * K,
+            "launches_per_step": launches_per_step,
+            "clocks": clk,
+            "wall_s_timed_loop": wall,
+        }
+        print(json.dumps(line), flush=True)
+    if dist:
+        dist.barrier()
+        dist.destroy_process_group()
+
+
+# arithmetic type of the expert path
+DTYPE = "f32"
+
+
+def main():
+    args = parse_args()
+    cfg = mi.CONFIGS[args.config]
+    if args.impl == "reference":
+        run_reference(args, cfg)
+    else:
+        run_ours(args, cfg)
+
+
+if __name__ == "__main__":
+    main()

@@ -1,0 +1,219 @@
+/*
+ * moe.h -- C ABI of libmoe: the routed MXFP4 mixture-of-experts block of a
+ * speculative-decode verify step, on one GB300 GPU (sm_103a), all experts
+ * resident, no collectives.
+ *
+ * The block (pages cited by their vLLM module names):
+ *   vllm.models.muse_spark.amd.mono.kernels.k3, stage list:
+ *     A      "router logits (fp32)"
+ *     route  "every CTA routes every token (identical top-8)"; route_token:
+ *            "sigmoid + ..." (the rest of that summary is cut off on the page)
+ *     C, D   "gate_up / down of the local experts: MXFP4 weights ..., decoded
+ *            in registers, bf16 MFMA"
+ *     E      "per-pick post-expert norm and weighted sum"
+ *   vllm.models.muse_spark.amd.mono.kernels.k5, HA: "router (fp32 ...) ...
+ *     top-8 ... h, top-k ids / weights for HM"
+ *   vllm.models.kimi_k3.amd.specialized_decode.mono.layer, k2_launch: the MoE
+ *     arguments w_gate, bias, w13, w13s, w2, w2s and "out the MoE output
+ *     [S, 7168]".
+ *
+ * What is computed, for token t (0 <= t < S):
+ *   L[t,e]   = sum_c x[t,c] * w_gate[e,c]  (fp32)  [+ logit_off[e]]
+ *   s[t,e]   = sigmoid(L[t,e]);  sel = s + bias[e]
+ *   picks    = the k experts with the largest sel (ties -> lower id),
+ *              reported in ascending expert id; weight w_j = s_j / sum_j s_j
+ *   g, u     = W1_e x_t, W3_e x_t   (W1 = rows 0..I-1 of w13, W3 = rows I..2I-1)
+ *   h        = silu(g) * u;   y = W2_e h
+ *   [post]   y <- y * rsqrt(mean(y^2) + norm_eps) * norm_w      (MOE_POST_NORM)
+ *   out[t]   = sum_j w_j * y_j                                      (fp32)
+ *
+ * MXFP4 encoding (OCP Microscaling v1.0): an e2m1 element is a 4-bit code
+ * (sign, 2 exponent bits with bias 1, 1 mantissa bit); an e8m0 scale byte b
+ * means 2^(b-127) and covers 32 consecutive K-elements of one row.  Packed
+ * rows are row-major with K contiguous: byte j holds element 2j in its low
+ * nibble and element 2j+1 in its high nibble.  Scale bytes 0..128 are
+ * supported (block scales 2^-127 .. 2^1, so that every weight is exact in
+ * bf16); a byte above 128 (255 is NaN in the MX format) latches
+ * MOE_ERR_BAD_SCALE on the device and its block is read as zero.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers (cudaMalloc'd or equivalent),
+ *     16-byte aligned, owned by the caller, and must stay valid until the
+ *     work queued on `stream` has finished.  Nothing is allocated, freed or
+ *     cached by the library on these paths; it keeps no state between calls
+ *     except per-device kernel attributes.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Calls only enqueue work; they do not synchronise, except
+ *     moe_device_status.
+ *   - `ws` is a device workspace of at least moe_workspace_bytes() bytes,
+ *     256-byte aligned, prepared once with moe_workspace_init.  Its first
+ *     bytes hold the device status word; calls that share one workspace must
+ *     be ordered on one stream.
+ *   - Return value: MOE_OK or a negative MOE_ERR_* code.  Host-side checks
+ *     (arguments, shape, alignment, workspace size) run before anything is
+ *     enqueued and enqueue nothing when they fail.  Errors found on the
+ *     device (bad ids, bad scale bytes, a bounded wait that ran out) are
+ *     latched in the workspace status word and reported by
+ *     moe_device_status.  The library never aborts, traps or asserts.
+ */
+#ifndef MOE_H
+#define MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+#define MOE_ABI_VERSION 1
+
+/* status codes */
+#define MOE_OK                     0
+#define MOE_ERR_INVALID_ARG       -1  /* NULL pointer, negative size, bad flags */
+#define MOE_ERR_UNSUPPORTED_SHAPE -2  /* shape outside the supported set (below) */
+#define MOE_ERR_ALIGNMENT         -3  /* a pointer is not 16-byte (ws: 256-byte) aligned */
+#define MOE_ERR_WORKSPACE         -4  /* ws_bytes < moe_workspace_bytes() */
+#define MOE_ERR_CUDA              -5  /* a CUDA runtime call or launch failed */
+#define MOE_ERR_TIMEOUT           -6  /* device: a bounded wait ran out */
+#define MOE_ERR_BAD_IDS           -7  /* device: an expert id outside [0, E) */
+#define MOE_ERR_BAD_SCALE         -8  /* device: an e8m0 byte above 128 */
+#define MOE_ERR_NO_DEVICE         -9  /* current device is not sm_103 (GB300) */
+
+/* moe_shape.flags */
+#define MOE_POST_NORM    1u  /* per-pick RMSNorm of y before the weighted sum */
+#define MOE_LOGIT_OFFSET 2u  /* add logit_off[e] to the router logits */
+
+/*
+ * Problem shape.  Supported: S >= 1, S * k <= 1<<20; d % 128 == 0 and
+ * 128 <= d <= 16384; I % 128 == 0 and 128 <= I <= 8192; 1 <= k <= 16;
+ * k <= E <= 512; norm_eps >= 0 (used with MOE_POST_NORM only).
+ */
+typedef struct moe_shape {
+    int32_t S;        /* token rows */
+    int32_t d;        /* hidden size (K of gate_up, N-rows of down) */
+    int32_t E;        /* experts */
+    int32_t k;        /* picks per token */
+    int32_t I;        /* expert intermediate size */
+    uint32_t flags;   /* MOE_POST_NORM | MOE_LOGIT_OFFSET */
+    float norm_eps;   /* RMSNorm epsilon */
+} moe_shape;
+
+/* ABI version of the loaded library (MOE_ABI_VERSION). */
+int moe_abi_version(void);
+
+/* Static English text for a status code; never NULL. */
+const char* moe_strerror(int code);
+
+/*
+ * Workspace size for `shape` in *bytes.  Returns MOE_OK, MOE_ERR_INVALID_ARG
+ * or MOE_ERR_UNSUPPORTED_SHAPE.  Pure host function.
+ */
+int moe_workspace_bytes(const moe_shape* shape, size_t* bytes);
+
+/*
+ * Clears the workspace's status block (enqueued on `stream`).  Call once after
+ * allocating a workspace, before its first use.
+ */
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Router + sigmoid top-k (k3 stages A and route; k5 HA).
+ *   x         [S, d]  bf16, row-major
+ *   w_gate    [E, d]  bf16, row-major (the router weight)
+ *   bias      [E]     fp32, selection bias (affects the choice, not w_j)
+ *   logit_off [E]     fp32, added to the logits when MOE_LOGIT_OFFSET is
+ *                     set, else ignored (may be NULL)
+ *   ids       [S, k]  int32 out: picks in ascending expert id
+ *   weights   [S, k]  fp32 out: renormalised sigmoid of the picks, aligned
+ *                     with ids
+ */
+int moe_route(const moe_shape* shape, const void* x, const void* w_gate,
+              const float* bias, const float* logit_off,
+              int32_t* ids, float* weights,
+              void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Experts + combine (k3 stages C, D, E; k2_launch w13/w13s/w2/w2s/out).
+ *   x         [S, d]        bf16
+ *   ids       [S, k]        int32, expert of each pick, distinct within a
+ *                           token, any order (an id outside [0, E), or one
+ *                           repeated within its token, latches
+ *                           MOE_ERR_BAD_IDS and that pick contributes
+ *                           nothing)
+ *   weights   [S, k]        fp32, aligned with ids
+ *   w13       [E, 2I, d/2]  packed e2m1; rows 0..I-1 gate, I..2I-1 up
+ *   w13s      [E, 2I, d/32] e8m0
+ *   w2        [E, d, I/2]   packed e2m1
+ *   w2s       [E, d, I/32]  e8m0
+ *   norm_w    [d]           fp32 post-expert norm weight (MOE_POST_NORM),
+ *                           else ignored (may be NULL)
+ *   out       [S, d]        fp32, overwritten
+ */
+int moe_experts(const moe_shape* shape, const void* x,
+                const int32_t* ids, const float* weights,
+                const uint8_t* w13, const uint8_t* w13s,
+                const uint8_t* w2, const uint8_t* w2s,
+                const float* norm_w, float* out,
+                void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * The whole block: moe_route then moe_experts on one stream, with the same
+ * arguments as those two (ids and weights are written, then consumed).
+ */
+int moe_forward(const moe_shape* shape, const void* x, const void* w_gate,
+                const float* bias, const float* logit_off,
+                const uint8_t* w13, const uint8_t* w13s,
+                const uint8_t* w2, const uint8_t* w2s,
+                const float* norm_w,
+                int32_t* ids, float* weights, float* out,
+                void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * moe_forward with the step's input and outputs in HOST memory:
+ *   x_host [S, d] bf16 is copied to the device inside the workspace, the block
+ *   runs, and ids_host [S, k], weights_host [S, k], out_host [S, d] are copied
+ *   back, all enqueued on `stream` (cudaMemcpyAsync; pinned host memory makes
+ *   them asynchronous).  The weights (w_gate, bias, logit_off, w13, w13s, w2,
+ *   w2s, norm_w) stay device pointers.  The host buffers must not be touched
+ *   until the stream has been synchronised.  ids_host / weights_host may be
+ *   NULL (then only out is copied back).
+ */
+int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_gate,
+                     const float* bias, const float* logit_off,
+                     const uint8_t* w13, const uint8_t* w13s,
+                     const uint8_t* w2, const uint8_t* w2s,
+                     const float* norm_w,
+                     int32_t* ids_host, float* weights_host, float* out_host,
+                     void* ws, size_t ws_bytes, void* stream);
+
+/*
+ * Synchronises `stream`, returns the status latched in the workspace by the
+ * device since the last call (MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_BAD_SCALE or
+ * MOE_ERR_TIMEOUT; MOE_ERR_CUDA if the synchronisation itself failed) and
+ * clears it.  *detail (may be NULL) receives a code-specific value: the first
+ * offending flat pick index, the first bad scale byte's value, or the site of
+ * the wait that ran out.
+ */
+int moe_device_status(void* ws, int32_t* detail, void* stream);
+
+/*
+ * Per-kernel timing (diagnostics, host side).  After moe_timing_enable(n) with
+ * n > 0, the next n kernels the library launches are each bracketed by a pair
+ * of CUDA events recorded on their launch stream; n = 0 turns this off and
+ * frees the events.  moe_timing_collect waits for the recorded events and
+ * writes up to `cap` (kernel id, milliseconds) pairs in launch order, the
+ * count to *n, and starts a new recording of the same size.  Kernel ids name
+ * the launched kernels (moe_kernel_name; NULL past the last id).  Not
+ * thread-safe; event records add a few microseconds of host time per launch.
+ * Returns MOE_OK, MOE_ERR_INVALID_ARG or MOE_ERR_CUDA.
+ */
+int moe_timing_enable(int max_launches);
+int moe_timing_collect(int32_t* kernel_ids, float* ms, int cap, int* n);
+const char* moe_kernel_name(int kernel_id);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MOE_H */

@@ -1,0 +1,273 @@
+// The C ABI of libmoe: argument checks, workspace layout and the launch order
+// of the block (router -> top-k -> expert sort/gather -> gate_up -> down ->
+// combine) on the caller's stream.  Declarations and contracts: include/moe.h.
+#include "moe_internal.cuh"
+
+#include <stdio.h>
+
+namespace moe {
+
+static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
+
+WsLayout ws_layout(const moe_shape& s) {
+    WsLayout L{};
+    const size_t P = (size_t)s.S * s.k;                  // picks
+    L.max_picks = (int)P;
+    L.max_tiles = (int)((P + NT - 1) / NT + s.E);        // >= sum_e ceil(n_e / NT)
+    size_t o = 0;
+    auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
+    L.status = take(sizeof(StatusBlock));
+    L.logits = take((size_t)s.S * s.E * 4);
+    L.counts = take((size_t)s.E * 4);
+    L.offsets = take((size_t)(s.E + 1) * 4);
+    L.pos = take(P * 4);
+    L.src = take(P * 4);
+    L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
+    L.active = take((size_t)s.E * 4);
+    L.xg = take(P * s.d * 2);
+    L.h = take(P * s.I * 2);
+    L.y = take(P * s.d * 4);
+    L.xin = take((size_t)s.S * s.d * 2);                 // host-I/O staging
+    L.hio_ids = take(P * 4);
+    L.hio_w = take(P * 4);
+    L.hio_out = take((size_t)s.S * s.d * 4);
+    L.total = o;
+    return L;
+}
+
+static int check_shape(const moe_shape* s) {
+    if (!s) return MOE_ERR_INVALID_ARG;
+    if (s->flags & ~(MOE_POST_NORM | MOE_LOGIT_OFFSET)) return MOE_ERR_INVALID_ARG;
+    if (s->S < 1 || s->d < 1 || s->E < 1 || s->k < 1 || s->I < 1) return MOE_ERR_INVALID_ARG;
+    if (!(s->norm_eps >= 0.0f)) return MOE_ERR_INVALID_ARG;
+    if (s->d % 128 || s->d > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (s->I % 128 || s->I > 8192) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (s->k > 16 || s->k > s->E || s->E > 512) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if ((int64_t)s->S * s->k > (1 << 20)) return MOE_ERR_UNSUPPORTED_SHAPE;
+    return MOE_OK;
+}
+
+static bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+
+static int check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)ws & 255) return MOE_ERR_ALIGNMENT;
+    if (ws_bytes < ws_layout(*s).total) return MOE_ERR_WORKSPACE;
+    return MOE_OK;
+}
+
+static int check_device() {
+    int dev = 0;
+    if (cudaGetDevice(&dev) != cudaSuccess) { cudaGetLastError(); return MOE_ERR_NO_DEVICE; }
+    int major = 0, minor = 0;
+    if (cudaDeviceGetAttribute(&major, cudaDevAttrComputeCapabilityMajor, dev) != cudaSuccess ||
+        cudaDeviceGetAttribute(&minor, cudaDevAttrComputeCapabilityMinor, dev) != cudaSuccess) {
+        cudaGetLastError();
+        return MOE_ERR_NO_DEVICE;
+    }
+    return (major == 10 && minor == 3) ? MOE_OK : MOE_ERR_NO_DEVICE;
+}
+
+static int cuda_rc(cudaError_t e) {
+    if (e == cudaSuccess) return MOE_OK;
+    fprintf(stderr, "libmoe: CUDA error %d (%s)\n", (int)e, cudaGetErrorString(e));
+    return MOE_ERR_CUDA;
+}
+
+static int check_route_args(const moe_shape* s, const void* x, const void* w_gate, const float* bias,
+                            const float* logit_off, const int32_t* ids, const float* w) {
+    if (!x || !w_gate || !bias || !ids || !w) return MOE_ERR_INVALID_ARG;
+    if ((s->flags & MOE_LOGIT_OFFSET) && !logit_off) return MOE_ERR_INVALID_ARG;
+    if (!a16(x) || !a16(w_gate) || !a16(bias) || !a16(ids) || !a16(w)) return MOE_ERR_ALIGNMENT;
+    if ((s->flags & MOE_LOGIT_OFFSET) && !a16(logit_off)) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+static int check_expert_args(const moe_shape* s, const void* x, const int32_t* ids, const float* w,
+                             const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                             const uint8_t* w2s, const float* norm_w, const float* out) {
+    if (!x || !ids || !w || !w13 || !w13s || !w2 || !w2s || !out) return MOE_ERR_INVALID_ARG;
+    if ((s->flags & MOE_POST_NORM) && !norm_w) return MOE_ERR_INVALID_ARG;
+    if (!a16(x) || !a16(ids) || !a16(w) || !a16(w13) || !a16(w13s) || !a16(w2) || !a16(w2s) || !a16(out))
+        return MOE_ERR_ALIGNMENT;
+    if ((s->flags & MOE_POST_NORM) && !a16(norm_w)) return MOE_ERR_ALIGNMENT;
+    return MOE_OK;
+}
+
+static int run_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    return cuda_rc(launch_route(s, L, p, st));
+}
+
+static int run_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    int rc = cuda_rc(launch_sort_gather(s, L, p, st));
+    if (rc) return rc;
+    rc = cuda_rc(launch_experts(s, L, p, st));
+    if (rc) return rc;
+    return cuda_rc(launch_combine(s, L, p, st));
+}
+
+}  // namespace moe
+
+using namespace moe;
+
+extern "C" {
+
+int moe_abi_version(void) { return MOE_ABI_VERSION; }
+
+const char* moe_strerror(int code) {
+    switch (code) {
+        case MOE_OK: return "ok";
+        case MOE_ERR_INVALID_ARG: return "invalid argument";
+        case MOE_ERR_UNSUPPORTED_SHAPE: return "unsupported shape";
+        case MOE_ERR_ALIGNMENT: return "misaligned pointer";
+        case MOE_ERR_WORKSPACE: return "workspace too small";
+        case MOE_ERR_CUDA: return "CUDA error";
+        case MOE_ERR_TIMEOUT: return "device wait timed out";
+        case MOE_ERR_BAD_IDS: return "expert id out of range or repeated within a token";
+        case MOE_ERR_BAD_SCALE: return "e8m0 scale byte above 128";
+        case MOE_ERR_NO_DEVICE: return "no sm_103 device";
+        default: return "unknown status";
+    }
+}
+
+int moe_workspace_bytes(const moe_shape* shape, size_t* bytes) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = ws_layout(*shape).total;
+    return MOE_OK;
+}
+
+int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)ws & 255) return MOE_ERR_ALIGNMENT;
+    if (ws_bytes < sizeof(StatusBlock)) return MOE_ERR_WORKSPACE;
+    int rc = check_device();
+    if (rc) return rc;
+    return cuda_rc(cudaMemsetAsync(ws, 0, sizeof(StatusBlock), (cudaStream_t)stream));
+}
+
+int moe_route(const moe_shape* shape, const void* x, const void* w_gate, const float* bias,
+              const float* logit_off, int32_t* ids, float* weights, void* ws, size_t ws_bytes,
+              void* stream) {
+    int rc = check_shape(shape);
+    if (!rc) rc = check_route_args(shape, x, w_gate, bias, logit_off, ids, weights);
+    if (!rc) rc = check_ws(shape, ws, ws_bytes);
+    if (!rc) rc = check_device();
+    if (rc) return rc;
+    WsLayout L = ws_layout(*shape);
+    Ptrs p{};
+    p.x = (const __nv_bfloat16*)x;
+    p.w_gate = (const __nv_bfloat16*)w_gate;
+    p.bias = bias;
+    p.logit_off = (shape->flags & MOE_LOGIT_OFFSET) ? logit_off : nullptr;
+    p.ids = ids;
+    p.weights = weights;
+    p.ws = (char*)ws;
+    return run_route(*shape, L, p, (cudaStream_t)stream);
+}
+
+int moe_experts(const moe_shape* shape, const void* x, const int32_t* ids, const float* weights,
+                const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2, const uint8_t* w2s,
+                const float* norm_w, float* out, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (!rc) rc = check_expert_args(shape, x, ids, weights, w13, w13s, w2, w2s, norm_w, out);
+    if (!rc) rc = check_ws(shape, ws, ws_bytes);
+    if (!rc) rc = check_device();
+    if (rc) return rc;
+    WsLayout L = ws_layout(*shape);
+    Ptrs p{};
+    p.x = (const __nv_bfloat16*)x;
+    p.ids = const_cast<int32_t*>(ids);
+    p.weights = const_cast<float*>(weights);
+    p.w13 = w13; p.w13s = w13s; p.w2 = w2; p.w2s = w2s;
+    p.norm_w = (shape->flags & MOE_POST_NORM) ? norm_w : nullptr;
+    p.out = out;
+    p.ws = (char*)ws;
+    return run_experts(*shape, L, p, (cudaStream_t)stream);
+}
+
+int moe_forward(const moe_shape* shape, const void* x, const void* w_gate, const float* bias,
+                const float* logit_off, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                const uint8_t* w2s, const float* norm_w, int32_t* ids, float* weights, float* out,
+                void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (!rc) rc = check_route_args(shape, x, w_gate, bias, logit_off, ids, weights);
+    if (!rc) rc = check_expert_args(shape, x, ids, weights, w13, w13s, w2, w2s, norm_w, out);
+    if (!rc) rc = check_ws(shape, ws, ws_bytes);
+    if (!rc) rc = check_device();
+    if (rc) return rc;
+    WsLayout L = ws_layout(*shape);
+    Ptrs p{};
+    p.x = (const __nv_bfloat16*)x;
+    p.w_gate = (const __nv_bfloat16*)w_gate;
+    p.bias = bias;
+    p.logit_off = (shape->flags & MOE_LOGIT_OFFSET) ? logit_off : nullptr;
+    p.w13 = w13; p.w13s = w13s; p.w2 = w2; p.w2s = w2s;
+    p.norm_w = (shape->flags & MOE_POST_NORM) ? norm_w : nullptr;
+    p.ids = ids;
+    p.weights = weights;
+    p.out = out;
+    p.ws = (char*)ws;
+    cudaStream_t st = (cudaStream_t)stream;
+    rc = run_route(*shape, L, p, st);
+    if (rc) return rc;
+    return run_experts(*shape, L, p, st);
+}
+
+int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_gate, const float* bias,
+                     const float* logit_off, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                     const uint8_t* w2s, const float* norm_w, int32_t* ids_host, float* weights_host,
+                     float* out_host, void* ws, size_t ws_bytes, void* stream) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (!x_host || !out_host) return MOE_ERR_INVALID_ARG;
+    if (!w_gate || !bias || !w13 || !w13s || !w2 || !w2s) return MOE_ERR_INVALID_ARG;
+    if ((shape->flags & MOE_LOGIT_OFFSET) && !logit_off) return MOE_ERR_INVALID_ARG;
+    if ((shape->flags & MOE_POST_NORM) && !norm_w) return MOE_ERR_INVALID_ARG;
+    if (!a16(w_gate) || !a16(bias) || !a16(w13) || !a16(w13s) || !a16(w2) || !a16(w2s))
+        return MOE_ERR_ALIGNMENT;
+    rc = check_ws(shape, ws, ws_bytes);
+    if (!rc) rc = check_device();
+    if (rc) return rc;
+    // device copies of the step's input and outputs live in the workspace's
+    // host-I/O staging regions (xin, hio_ids, hio_w, hio_out)
+    WsLayout L = ws_layout(*shape);
+    cudaStream_t st = (cudaStream_t)stream;
+    char* w = (char*)ws;
+    const size_t P = (size_t)shape->S * shape->k;
+    void* x_dev = w + L.xin;
+    rc = cuda_rc(cudaMemcpyAsync(x_dev, x_host, (size_t)shape->S * shape->d * 2, cudaMemcpyHostToDevice, st));
+    if (rc) return rc;
+    int32_t* ids_dev = (int32_t*)(w + L.hio_ids);
+    float* wts_dev = (float*)(w + L.hio_w);
+    float* out_dev = (float*)(w + L.hio_out);
+    rc = moe_forward(shape, x_dev, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids_dev, wts_dev,
+                     out_dev, ws, ws_bytes, stream);
+    if (rc) return rc;
+    rc = cuda_rc(cudaMemcpyAsync(out_host, out_dev, (size_t)shape->S * shape->d * 4, cudaMemcpyDeviceToHost, st));
+    if (!rc && ids_host)
+        rc = cuda_rc(cudaMemcpyAsync(ids_host, ids_dev, P * 4, cudaMemcpyDeviceToHost, st));
+    if (!rc && weights_host)
+        rc = cuda_rc(cudaMemcpyAsync(weights_host, wts_dev, P * 4, cudaMemcpyDeviceToHost, st));
+    return rc;
+}
+
+int moe_device_status(void* ws, int32_t* detail, void* stream) {
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)ws & 255) return MOE_ERR_ALIGNMENT;
+    cudaStream_t st = (cudaStream_t)stream;
+    StatusBlock hb{};
+    if (cudaStreamSynchronize(st) != cudaSuccess) return cuda_rc(cudaGetLastError());
+    if (cudaMemcpy(&hb, ws, 2 * sizeof(int32_t), cudaMemcpyDeviceToHost) != cudaSuccess)
+        return cuda_rc(cudaGetLastError());
+    if (hb.status != 0) {
+        int32_t zero[2] = {0, 0};
+        if (cudaMemcpy(ws, zero, sizeof(zero), cudaMemcpyHostToDevice) != cudaSuccess)
+            return cuda_rc(cudaGetLastError());
+    }
+    if (detail) *detail = hb.detail;
+    return hb.status;
+}
+
+}  // extern "C"

@@ -1,0 +1,85 @@
+// Internal declarations shared by the translation units of libmoe.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <cuda_bf16.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace moe {
+
+// ---------------------------------------------------------------------------
+// device status block (first 256 bytes of the workspace)
+// ---------------------------------------------------------------------------
+struct StatusBlock {
+    int32_t status;     // first latched MOE_ERR_* (0 = none)
+    int32_t detail;     // code-specific detail of that error
+    int32_t n_picks;    // valid picks of the current call (written by the sort)
+    int32_t n_tiles;    // gate_up work tiles of the current call
+    int32_t n_active;   // experts with at least one pick
+    int32_t work_next;  // persistent-kernel work counters (reset each call)
+    int32_t work_next2;
+    int32_t pad[57];
+};
+static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
+
+// Token-tile width of the expert GEMMs: one tile holds up to NT picks of one
+// expert (the MMA N dimension; the pages' 16-row tiles, k5 page).
+constexpr int NT = 16;
+
+// One work tile: expert e, first sorted pick p0, n picks (n <= NT).
+struct Tile {
+    int32_t e, p0, n, pad;
+};
+
+// Byte offsets of the workspace regions (all 256-byte aligned).
+struct WsLayout {
+    size_t status, logits, counts, offsets, pos, src, tiles, active, xg, h, y;
+    size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
+    size_t total;
+    int max_tiles;
+    int max_picks;
+};
+
+WsLayout ws_layout(const moe_shape& s);
+
+__device__ __forceinline__ void latch_status(StatusBlock* sb, int code, int detail) {
+    if (atomicCAS(&sb->status, 0, code) == 0) sb->detail = detail;
+}
+
+// ---------------------------------------------------------------------------
+// per-kernel timing hooks (moe_timing_*): no-ops unless enabled
+// ---------------------------------------------------------------------------
+enum KernelId {
+    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_GATEUP, K_DOWN, K_COMBINE, K_NUM
+};
+void timing_begin(int kernel_id, cudaStream_t st);
+void timing_end(cudaStream_t st);
+
+// ---------------------------------------------------------------------------
+// launchers (one per kernel); all return cudaGetLastError() of the launch
+// ---------------------------------------------------------------------------
+struct Ptrs {
+    const __nv_bfloat16* x;
+    const __nv_bfloat16* w_gate;
+    const float* bias;
+    const float* logit_off;
+    const uint8_t* w13;
+    const uint8_t* w13s;
+    const uint8_t* w2;
+    const uint8_t* w2s;
+    const float* norm_w;
+    int32_t* ids;
+    float* weights;
+    float* out;
+    char* ws;
+};
+
+cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+
+}  // namespace moe

@@ -1,0 +1,226 @@
+// Expert sort, work-tile schedule and token gather.
+//
+// vllm.models.muse_spark.amd.mono.kernels.k3, dn_loads: "Task (u, j)'s w2
+// operands ... expert etab[u], u clamped below nv" -- the pages keep a table of
+// the local experts that have picks and run tasks (expert, tile).  Here that
+// table is built once per call: picks are counted per expert, sorted by
+// (expert, token) with a stable counting sort, and cut into tiles of at most
+// NT picks of one expert (k5 page: "Every row tile is 16 tokens").  Experts
+// without picks get no tile, so no weight byte of an untouched expert is read.
+#include "moe_internal.cuh"
+
+namespace moe {
+
+namespace {
+
+constexpr int SORT_THREADS = 1024;
+constexpr int SORT_WARPS = SORT_THREADS / 32;
+constexpr int MAX_K = 16;
+
+// One CTA.  Warp w owns the token range [w*tpw, (w+1)*tpw) (tpw a multiple of
+// 32) and walks it in groups of 32 tokens, lane = token.
+//   pass 1: validate ids, per-warp per-expert counts (smem)
+//   pass 2: per-expert exclusive scan over warps, scan over experts -> offsets,
+//           tile schedule, active list
+//   pass 3: positions: offset[e] + base[w][e] + rank among earlier tokens of
+//           the group that picked e (a 32-bit lane mask per expert)
+// Output: counts[E], offsets[E+1], pos[t*k+j] (-1 for an invalid pick),
+// src[p] = t*k+j, tiles[], active[], and n_picks / n_tiles / n_active.
+__global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict__ ids, int S, int E, int k,
+                                                       int32_t* __restrict__ counts,
+                                                       int32_t* __restrict__ offsets,
+                                                       int32_t* __restrict__ pos, int32_t* __restrict__ src,
+                                                       Tile* __restrict__ tiles, int32_t* __restrict__ active,
+                                                       StatusBlock* __restrict__ sb) {
+    extern __shared__ int32_t smem[];
+    int32_t* cnt = smem;                        // [SORT_WARPS][E]
+    uint32_t* mask = reinterpret_cast<uint32_t*>(smem + SORT_WARPS * E);  // [SORT_WARPS][E]
+    int32_t* etot = smem + 2 * SORT_WARPS * E;  // [E] totals, then exclusive offsets
+    int32_t* etil = etot + E;                   // [E] tiles per expert, then tile offsets
+    int32_t* eact = etil + E;                   // [E] active flag, then active slot
+    __shared__ int32_t scan_tmp[SORT_THREADS / 32];
+
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+    for (int i = tid; i < 2 * SORT_WARPS * E; i += SORT_THREADS) smem[i] = 0;
+    __syncthreads();
+
+    const int groups = (S + 31) / 32;
+    const int gpw = (groups + SORT_WARPS - 1) / SORT_WARPS;   // groups per warp
+    const int g0 = warp * gpw, g1 = min(groups, g0 + gpw);
+
+    // pass 1 ------------------------------------------------------------
+    for (int g = g0; g < g1; ++g) {
+        const int t = g * 32 + lane;
+        if (t < S) {
+            int my[MAX_K];
+            uint32_t valid = 0;
+            for (int j = 0; j < k; ++j) {
+                const int e = ids[(size_t)t * k + j];
+                my[j] = e;
+                bool ok = (e >= 0 && e < E);
+                for (int q = 0; q < j; ++q) ok = ok && (my[q] != e);
+                if (ok) {
+                    valid |= 1u << j;
+                    atomicAdd(&cnt[warp * E + e], 1);
+                } else {
+                    latch_status(sb, MOE_ERR_BAD_IDS, t * k + j);
+                }
+            }
+        }
+    }
+    __syncthreads();
+
+    // pass 2 ------------------------------------------------------------
+    for (int e = tid; e < E; e += SORT_THREADS) {
+        int run = 0;
+        for (int w = 0; w < SORT_WARPS; ++w) {
+            const int c = cnt[w * E + e];
+            cnt[w * E + e] = run;
+            run += c;
+        }
+        etot[e] = run;
+        etil[e] = (run + NT - 1) / NT;
+        eact[e] = run > 0 ? 1 : 0;
+    }
+    __syncthreads();
+    // three exclusive scans over E (E <= 512 < SORT_THREADS): one element per thread
+    auto block_scan = [&](int32_t* a, int32_t* total) {
+        const int v = tid < E ? a[tid] : 0;
+        int inc = v;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int o = __shfl_up_sync(0xffffffffu, inc, m);
+            if (lane >= m) inc += o;
+        }
+        if (lane == 31) scan_tmp[warp] = inc;
+        __syncthreads();
+        if (warp == 0) {
+            int w = scan_tmp[lane];
+            int wi = w;
+#pragma unroll
+            for (int m = 1; m < 32; m <<= 1) {
+                const int o = __shfl_up_sync(0xffffffffu, wi, m);
+                if (lane >= m) wi += o;
+            }
+            scan_tmp[lane] = wi - w;   // exclusive prefix of warp sums
+            if (lane == 31) *total = wi;
+        }
+        __syncthreads();
+        if (tid < E) a[tid] = scan_tmp[warp] + inc - v;
+        __syncthreads();
+    };
+    __shared__ int32_t tot_picks, tot_tiles, tot_active;
+    if (tid < E) counts[tid] = etot[tid];
+    __syncthreads();
+    block_scan(etot, &tot_picks);
+    block_scan(etil, &tot_tiles);
+    block_scan(eact, &tot_active);
+    for (int e = tid; e < E; e += SORT_THREADS) {
+        const int n = counts[e];
+        offsets[e] = etot[e];
+        if (n > 0) active[eact[e]] = e;
+        for (int i = 0, tb = etil[e]; i * NT < n; ++i) {
+            Tile tl;
+            tl.e = e;
+            tl.p0 = etot[e] + i * NT;
+            tl.n = min(NT, n - i * NT);
+            tl.pad = 0;
+            tiles[tb + i] = tl;
+        }
+    }
+    if (tid == 0) {
+        offsets[E] = tot_picks;
+        sb->n_picks = tot_picks;
+        sb->n_tiles = tot_tiles;
+        sb->n_active = tot_active;
+        sb->work_next = 0;
+        sb->work_next2 = 0;
+    }
+    __syncthreads();
+
+    // pass 3 ------------------------------------------------------------
+    const uint32_t lt = (1u << lane) - 1u;
+    for (int g = g0; g < g1; ++g) {
+        const int t = g * 32 + lane;
+        int my[MAX_K];
+        uint32_t valid = 0;
+        if (t < S) {
+            for (int j = 0; j < k; ++j) {
+                const int e = ids[(size_t)t * k + j];
+                my[j] = e;
+                bool ok = (e >= 0 && e < E);
+                for (int q = 0; q < j; ++q) ok = ok && (my[q] != e);
+                if (ok) {
+                    valid |= 1u << j;
+                    atomicOr(&mask[warp * E + e], 1u << lane);
+                } else {
+                    pos[(size_t)t * k + j] = -1;
+                }
+            }
+        }
+        __syncwarp();
+        int rank0[MAX_K];
+        for (int j = 0; j < k; ++j) {
+            rank0[j] = -1;
+            if (valid >> j & 1u) {
+                const int e = my[j];
+                const uint32_t m = mask[warp * E + e];
+                const int r = __popc(m & lt);
+                const int p = offsets[e] + cnt[warp * E + e] + r;
+                pos[(size_t)t * k + j] = p;
+                src[p] = t * k + j;
+                rank0[j] = (r == 0) ? __popc(m) : -1;
+            }
+        }
+        __syncwarp();
+        for (int j = 0; j < k; ++j) {
+            if (rank0[j] >= 0) {
+                const int e = my[j];
+                cnt[warp * E + e] += rank0[j];
+                mask[warp * E + e] = 0u;
+            }
+        }
+        __syncwarp();
+    }
+}
+
+// xg[p, :] = x[src[p] / k, :] for the valid picks p < n_picks.
+// grid (max_picks), 128 threads, 16-byte copies.
+__global__ void __launch_bounds__(128) k_gather(const __nv_bfloat16* __restrict__ x,
+                                                const int32_t* __restrict__ src, int k, int d,
+                                                __nv_bfloat16* __restrict__ xg,
+                                                const StatusBlock* __restrict__ sb) {
+    const int p = blockIdx.x;
+    if (p >= sb->n_picks) return;
+    const int t = src[p] / k;
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    uint4* o = reinterpret_cast<uint4*>(xg + (size_t)p * d);
+    for (int c = threadIdx.x; c < d / 8; c += blockDim.x) o[c] = __ldg(in + c);
+}
+
+}  // namespace
+
+cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    char* ws = p.ws;
+    StatusBlock* sb = reinterpret_cast<StatusBlock*>(ws + L.status);
+    const size_t smem = (size_t)(2 * SORT_WARPS * s.E + 3 * s.E) * sizeof(int32_t);
+    cudaError_t e = cudaFuncSetAttribute(k_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    timing_begin(K_SORT, st);
+    k_sort<<<1, SORT_THREADS, smem, st>>>(p.ids, s.S, s.E, s.k, reinterpret_cast<int32_t*>(ws + L.counts),
+                                          reinterpret_cast<int32_t*>(ws + L.offsets),
+                                          reinterpret_cast<int32_t*>(ws + L.pos),
+                                          reinterpret_cast<int32_t*>(ws + L.src),
+                                          reinterpret_cast<Tile*>(ws + L.tiles),
+                                          reinterpret_cast<int32_t*>(ws + L.active), sb);
+    timing_end(st);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    timing_begin(K_GATHER, st);
+    k_gather<<<L.max_picks, 128, 0, st>>>(p.x, reinterpret_cast<const int32_t*>(ws + L.src), s.k, s.d,
+                                          reinterpret_cast<__nv_bfloat16*>(ws + L.xg), sb);
+    timing_end(st);
+    return cudaGetLastError();
+}
+
+}  // namespace moe
