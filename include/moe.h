@@ -188,6 +188,37 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
                      void* ws, size_t ws_bytes, void* stream);
 
 /*
+ * moe_forward without a workspace argument, for callers that cannot allocate
+ * device memory where they run the block (an operator or plugin interface
+ * that passes only inputs and outputs, an application whose memory pool owns
+ * the whole GPU, a serving loop that must not call cudaMalloc).  The pages have
+ * no counterpart: their launchers always receive a scratch buffer.
+ *
+ * Scratch comes from a 32 MiB static device array inside the library, which
+ * every GPU that loads the library holds until the process exits.  Shapes
+ * whose moe_workspace_bytes() exceeds 32 MiB are rejected with
+ * MOE_ERR_WORKSPACE before anything is enqueued (S * k <= 256 at d = 4096,
+ * I = 1024, E = 256 fits).  No call allocates or frees memory.  The first call
+ * on a device looks up the array's device address once (cudaGetSymbolAddress,
+ * with that device current); make that first call before any stream capture.
+ *
+ * Every call on a device shares the one array, which keeps the previous
+ * call's contents; each call clears its status block first.  Calls that
+ * overlap on the GPU (other streams, other host threads) race on the array:
+ * order them on one stream.  Arguments are those of moe_forward minus the
+ * workspace; `status` (device int32[2], may be NULL) receives this call's
+ * device status and detail (see moe_device_status) when the call's work is
+ * done.
+ */
+int moe_forward_noalloc(const moe_shape* shape, const void* x, const void* w_gate,
+                        const float* bias, const float* logit_off,
+                        const uint8_t* w13, const uint8_t* w13s,
+                        const uint8_t* w2, const uint8_t* w2s,
+                        const float* norm_w,
+                        int32_t* ids, float* weights, float* out,
+                        int32_t* status, void* stream);
+
+/*
  * Synchronises `stream`, returns the status latched in the workspace by the
  * device since the last call (MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_BAD_SCALE or
  * MOE_ERR_TIMEOUT; MOE_ERR_CUDA if the synchronisation itself failed) and

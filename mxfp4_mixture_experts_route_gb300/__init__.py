@@ -31,7 +31,7 @@ MOE_LOGIT_OFFSET = 2
 # every symbol include/moe.h declares
 EXPORTS = ("moe_abi_version", "moe_strerror", "moe_workspace_bytes", "moe_workspace_init",
            "moe_route", "moe_experts", "moe_forward", "moe_forward_host", "moe_device_status",
-           "moe_timing_enable", "moe_timing_collect", "moe_kernel_name")
+           "moe_timing_enable", "moe_timing_collect", "moe_kernel_name", "moe_forward_noalloc")
 
 
 class MoEShape(ctypes.Structure):
@@ -79,6 +79,7 @@ def lib() -> ctypes.CDLL:
         L.moe_forward.argtypes = [_SP] + [_P] * 13 + [ctypes.c_size_t, _P]
         L.moe_forward_host.argtypes = [_SP] + [_P] * 13 + [ctypes.c_size_t, _P]
         L.moe_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+        L.moe_forward_noalloc.argtypes = [_SP] + [_P] * 14
         L.moe_timing_enable.argtypes = [ctypes.c_int]
         L.moe_timing_collect.argtypes = [_P, _P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
         L.moe_kernel_name.argtypes = [ctypes.c_int]
