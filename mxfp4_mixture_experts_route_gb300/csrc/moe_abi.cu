@@ -13,7 +13,8 @@ WsLayout ws_layout(const moe_shape& s) {
     WsLayout L{};
     const size_t P = (size_t)s.S * s.k;                  // picks
     L.max_picks = (int)P;
-    L.max_tiles = (int)((P + NT - 1) / NT + s.E);        // >= sum_e ceil(n_e / NT)
+    // sum_e ceil(n_e / NT) <= P / NT + (experts with a pick) <= ceil(P / NT) + min(E, P)
+    L.max_tiles = (int)((P + NT - 1) / NT + (P < (size_t)s.E ? P : (size_t)s.E));
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(sizeof(StatusBlock));
@@ -24,6 +25,7 @@ WsLayout ws_layout(const moe_shape& s) {
     L.src = take(P * 4);
     L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
     L.active = take((size_t)s.E * 4);
+    L.tile_ready = take((size_t)L.max_tiles * 4);
     L.xg = take(P * s.d * 2);
     L.h = take(P * s.I * 2);
     L.y = take(P * s.d * 4);

@@ -36,7 +36,7 @@ struct Tile {
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, logits, counts, offsets, pos, src, tiles, active, xg, h, y;
+    size_t status, logits, counts, offsets, pos, src, tiles, active, tile_ready, xg, h, y;
     size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
     size_t total;
     int max_tiles;
@@ -53,7 +53,7 @@ __device__ __forceinline__ void latch_status(StatusBlock* sb, int code, int deta
 // per-kernel timing hooks (moe_timing_*): no-ops unless enabled
 // ---------------------------------------------------------------------------
 enum KernelId {
-    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_GATEUP, K_DOWN, K_COMBINE, K_NUM
+    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_NUM
 };
 void timing_begin(int kernel_id, cudaStream_t st);
 void timing_end(cudaStream_t st);

@@ -31,6 +31,7 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
                                                        int32_t* __restrict__ offsets,
                                                        int32_t* __restrict__ pos, int32_t* __restrict__ src,
                                                        Tile* __restrict__ tiles, int32_t* __restrict__ active,
+                                                       uint32_t* __restrict__ tile_ready, int max_tiles,
                                                        StatusBlock* __restrict__ sb) {
     extern __shared__ int32_t smem[];
     int32_t* cnt = smem;                        // [SORT_WARPS][E]
@@ -42,6 +43,7 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < 2 * SORT_WARPS * E; i += SORT_THREADS) smem[i] = 0;
+    for (int i = tid; i < max_tiles; i += SORT_THREADS) tile_ready[i] = 0u;
     __syncthreads();
 
     const int groups = (S + 31) / 32;
@@ -184,8 +186,10 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
     }
 }
 
-// xg[p, :] = x[src[p] / k, :] for the valid picks p < n_picks.
-// grid (max_picks), 128 threads, 16-byte copies.
+// xg[p, :] = x[src[p] / k, :] for the valid picks p < n_picks, with the K
+// order inside every group of 8 elements rearranged to the MMA order of the
+// expert kernel's weight decode: positions (0..7) hold elements
+// (0, 4, 1, 5, 2, 6, 3, 7).  grid (max_picks), 128 threads, 16-byte copies.
 __global__ void __launch_bounds__(128) k_gather(const __nv_bfloat16* __restrict__ x,
                                                 const int32_t* __restrict__ src, int k, int d,
                                                 __nv_bfloat16* __restrict__ xg,
@@ -195,7 +199,15 @@ __global__ void __launch_bounds__(128) k_gather(const __nv_bfloat16* __restrict_
     const int t = src[p] / k;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     uint4* o = reinterpret_cast<uint4*>(xg + (size_t)p * d);
-    for (int c = threadIdx.x; c < d / 8; c += blockDim.x) o[c] = __ldg(in + c);
+    for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
+        const uint4 v = __ldg(in + c);
+        uint4 w;
+        w.x = __byte_perm(v.x, v.z, 0x5410);   // elements 0, 4
+        w.y = __byte_perm(v.x, v.z, 0x7632);   // elements 1, 5
+        w.z = __byte_perm(v.y, v.w, 0x5410);   // elements 2, 6
+        w.w = __byte_perm(v.y, v.w, 0x7632);   // elements 3, 7
+        o[c] = w;
+    }
 }
 
 }  // namespace
@@ -212,7 +224,8 @@ cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs
                                           reinterpret_cast<int32_t*>(ws + L.pos),
                                           reinterpret_cast<int32_t*>(ws + L.src),
                                           reinterpret_cast<Tile*>(ws + L.tiles),
-                                          reinterpret_cast<int32_t*>(ws + L.active), sb);
+                                          reinterpret_cast<int32_t*>(ws + L.active),
+                                          reinterpret_cast<uint32_t*>(ws + L.tile_ready), L.max_tiles, sb);
     timing_end(st);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
