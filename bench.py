@@ -156,8 +156,7 @@ def algorithmic_bytes(cfg: mi.MoEConfig, n_touched: int) -> dict:
     per_w13 = 2 * cfg.I * cfg.d * 17 // 32
     per_w2 = cfg.d * cfg.I * 17 // 32
     return {
-        "gateup": n_touched * per_w13,
-        "down": n_touched * per_w2,
+        "experts": n_touched * (per_w13 + per_w2),
         "router_logits": cfg.E * cfg.d * 2 + cfg.S * cfg.d * 2,
         "step": n_touched * (per_w13 + per_w2) + cfg.E * cfg.d * 2 + 4 * cfg.E,
     }
@@ -376,8 +375,8 @@ def run_ours(args, cfg: mi.MoEConfig):
         dist.destroy_process_group()
 
 
-# arithmetic type of the expert path
-DTYPE = "f32"
+# arithmetic type of the expert path: bf16 tensor-core MMA (fp32 accumulate)
+DTYPE = "bf16"
 
 
 def main():
