@@ -18,7 +18,10 @@ WsLayout ws_layout(const moe_shape& s) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(sizeof(StatusBlock));
-    L.logits = take((size_t)s.S * s.E * 4);
+    // router partial logits: the K-range count is chosen for 152 SMs (GB300);
+    // another SM count only changes how the work is split
+    L.router_kslices = router_kslices(s, 152);
+    L.logits = take((size_t)L.router_kslices * s.S * s.E * 4);
     L.counts = take((size_t)s.E * 4);
     L.offsets = take((size_t)(s.E + 1) * 4);
     L.pos = take(P * 4);

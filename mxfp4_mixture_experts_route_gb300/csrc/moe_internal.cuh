@@ -41,9 +41,11 @@ struct WsLayout {
     size_t total;
     int max_tiles;
     int max_picks;
+    int router_kslices;   // K-ranges of the router's partial logits
 };
 
 WsLayout ws_layout(const moe_shape& s);
+int router_kslices(const moe_shape& s, int num_sms);
 
 __device__ __forceinline__ void latch_status(StatusBlock* sb, int code, int detail) {
     if (atomicCAS(&sb->status, 0, code) == 0) sb->detail = detail;
