@@ -12,74 +12,87 @@ namespace moe {
 namespace {
 
 constexpr int CB_THREADS = 256;
+constexpr int CB_COLS = 4 * CB_THREADS;   // columns of out per CTA
+constexpr int CB_MAXK = 16;               // picks per token (k <= 16)
 
-// one CTA per token; y rows of the token's picks are read from the sorted
-// per-pick buffer through pos[t*k + j]
-__global__ void __launch_bounds__(CB_THREADS) k_combine(const float* __restrict__ y,
-                                                        const int32_t* __restrict__ pos,
-                                                        const float* __restrict__ w, const float* __restrict__ norm_w,
-                                                        float eps, int k, int d, float* __restrict__ out) {
+// grid (S, ceil(d / 1024)): CTA (t, c) writes out[t, 1024c .. 1024c+1023] =
+// sum_j coef_j * y[pos(t, j), cols] (* norm_w[cols]), with coef_j = w_j, or
+// for the post-expert norm w_j * rsqrt(mean(y_j^2) + eps).  y_j's sum of
+// squares comes from the per-128-row-block sums the down GEMM's epilogue
+// writes: warp w adds up the blocks of picks w and w + 8 (lanes over blocks,
+// then a fixed shuffle tree), so the CTA never reads a whole y row twice.
+// y rows are addressed through pos[t*k + j] (the sorted per-pick buffer).
+__global__ void __launch_bounds__(CB_THREADS) k_combine(const float* __restrict__ y, const float* __restrict__ ssq,
+                                                        const int32_t* __restrict__ pos, const float* __restrict__ w,
+                                                        const float* __restrict__ norm_w, float eps, int k, int d,
+                                                        float* __restrict__ out) {
     const int t = blockIdx.x;
-    __shared__ float coef[16];
-    __shared__ int32_t prow[16];
-    __shared__ float red[CB_THREADS / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    for (int j = 0; j < k; ++j) {
-        const int p = pos[(size_t)t * k + j];
-        float c = (p >= 0) ? w[(size_t)t * k + j] : 0.f;
-        if (norm_w != nullptr && p >= 0) {
-            const float4* yr = reinterpret_cast<const float4*>(y + (size_t)p * d);
-            float ss = 0.f;
-            for (int i = tid; i < d / 4; i += CB_THREADS) {
-                const float4 v = yr[i];
-                ss += v.x * v.x + v.y * v.y + v.z * v.z + v.w * v.w;
-            }
+    __shared__ float coef[CB_MAXK];
+    __shared__ int32_t prow[CB_MAXK];
+    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
 #pragma unroll
-            for (int m = 16; m >= 1; m >>= 1) ss += __shfl_xor_sync(0xffffffffu, ss, m);
-            if (lane == 0) red[warp] = ss;
-            __syncthreads();
-            if (tid == 0) {
-                float tot = 0.f;
-                for (int i = 0; i < CB_THREADS / 32; ++i) tot += red[i];
-                coef[j] = c * rsqrtf(tot / (float)d + eps);
+    for (int h = 0; h < CB_MAXK / 8; ++h) {
+        const int j = warp + 8 * h;
+        if (j < k) {
+            const int p = pos[(size_t)t * k + j];
+            float c = w[(size_t)t * k + j];
+            if (norm_w != nullptr && p >= 0) {
+                const int nb = d / 128;                // <= 128 row blocks
+                float q = 0.f;
+#pragma unroll
+                for (int i = 0; i < 4; ++i) {
+                    const int b = lane + 32 * i;
+                    if (b < nb) q += ssq[(size_t)p * nb + b];
+                }
+#pragma unroll
+                for (int m = 16; m >= 1; m >>= 1) q += __shfl_xor_sync(0xffffffffu, q, m);
+                c *= rsqrtf(q / (float)d + eps);
             }
-            __syncthreads();
-        } else if (tid == 0) {
-            coef[j] = c;
+            if (lane == 0) {
+                coef[j] = p >= 0 ? c : 0.f;
+                prow[j] = p;
+            }
         }
-        if (tid == 0) prow[j] = p;
     }
     __syncthreads();
-    for (int i = tid; i < d / 4; i += CB_THREADS) {
-        float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-        for (int j = 0; j < k; ++j) {
-            const int p = prow[j];
-            if (p < 0) continue;
-            const float4 v = reinterpret_cast<const float4*>(y + (size_t)p * d)[i];
-            const float c = coef[j];
-            acc.x = fmaf(c, v.x, acc.x);
-            acc.y = fmaf(c, v.y, acc.y);
-            acc.z = fmaf(c, v.z, acc.z);
-            acc.w = fmaf(c, v.w, acc.w);
-        }
-        if (norm_w != nullptr) {
-            const float4 nw = reinterpret_cast<const float4*>(norm_w)[i];
-            acc.x *= nw.x;
-            acc.y *= nw.y;
-            acc.z *= nw.z;
-            acc.w *= nw.w;
-        }
-        reinterpret_cast<float4*>(out + (size_t)t * d)[i] = acc;
+    const int col = blockIdx.y * CB_COLS + 4 * tid;
+    if (col >= d) return;
+    float4 v[CB_MAXK];
+#pragma unroll
+    for (int j = 0; j < CB_MAXK; ++j) {           // every pick's load in flight at once
+        v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (j < k && prow[j] >= 0) v[j] = *reinterpret_cast<const float4*>(y + (size_t)prow[j] * d + col);
     }
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int j = 0; j < CB_MAXK; ++j) {           // summed in pick order j
+        if (j < k) {
+            const float c = coef[j];
+            acc.x = fmaf(c, v[j].x, acc.x);
+            acc.y = fmaf(c, v[j].y, acc.y);
+            acc.z = fmaf(c, v[j].z, acc.z);
+            acc.w = fmaf(c, v[j].w, acc.w);
+        }
+    }
+    if (norm_w != nullptr) {
+        const float4 nw = *reinterpret_cast<const float4*>(norm_w + col);
+        acc.x *= nw.x;
+        acc.y *= nw.y;
+        acc.z *= nw.z;
+        acc.w *= nw.w;
+    }
+    *reinterpret_cast<float4*>(out + (size_t)t * d + col) = acc;
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     timing_begin(K_COMBINE, st);
-    k_combine<<<s.S, CB_THREADS, 0, st>>>(reinterpret_cast<const float*>(p.ws + L.y),
-                                          reinterpret_cast<const int32_t*>(p.ws + L.pos), p.weights, p.norm_w,
-                                          s.norm_eps, s.k, s.d, p.out);
+    const dim3 grid(s.S, (s.d + CB_COLS - 1) / CB_COLS);
+    k_combine<<<grid, CB_THREADS, 0, st>>>(reinterpret_cast<const float*>(p.ws + L.y),
+                                           reinterpret_cast<const float*>(p.ws + L.ssq),
+                                           reinterpret_cast<const int32_t*>(p.ws + L.pos), p.weights, p.norm_w,
+                                           s.norm_eps, s.k, s.d, p.out);
     timing_end(st);
     return cudaGetLastError();
 }

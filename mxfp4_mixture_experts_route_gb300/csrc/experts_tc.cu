@@ -124,6 +124,7 @@ struct Args {
     const uint8_t* w2s;
     __nv_bfloat16* h;
     float* y;
+    float* ssq;      // per-pick sums of y^2 by 128-row block, or null
     uint32_t* tile_ready;
     int d, I;
 };
@@ -629,6 +630,43 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                 for (int n = 0; n < N; ++n)
                     if (n < U.n) a.y[(size_t)(U.p0 + n) * a.d + m] = v[n];
+                if (a.ssq != nullptr) {
+                    // sum of y^2 over the unit's 128 rows for every pick: a
+                    // reduce-scatter across the warp (lane l ends with picks
+                    // [idx, idx + c)), then the four warps' sums in warp order
+                    float q[N];
+#pragma unroll
+                    for (int n = 0; n < N; ++n) q[n] = v[n] * v[n];
+                    int idx = 0;
+#pragma unroll
+                    for (int step = 0; step < 5; ++step) {
+                        const int o = 16 >> step;
+                        const int c = N >> step;        // values a lane holds before this step
+                        const bool hi = (lane & o) != 0;
+                        if (c > 1) {
+#pragma unroll
+                            for (int j = 0; j < c / 2; ++j) {
+                                const float send = hi ? q[j] : q[j + c / 2];
+                                const float keep = hi ? q[j + c / 2] : q[j];
+                                q[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                            }
+                            idx += hi ? c / 2 : 0;
+                        } else {
+                            q[0] += __shfl_xor_sync(0xffffffffu, q[0], o);
+                        }
+                    }
+                    constexpr int C_END = N >= 32 ? N / 32 : 1;   // values a lane holds at the end
+                    constexpr int SHARE = 32 * C_END / N;          // lanes holding the same values
+                    float* part = xch;                             // [4][N]
+                    if (lane % SHARE == 0) {
+#pragma unroll
+                        for (int j = 0; j < C_END; ++j) part[qd * N + idx + j] = q[j];
+                    }
+                    ptx::named_bar_sync(1, 128);
+                    if (r < U.n)
+                        a.ssq[(size_t)(U.p0 + r) * (a.d / AROWS) + U.mb] =
+                            ((part[r] + part[N + r]) + part[2 * N + r]) + part[3 * N + r];
+                }
             }
         }
     }
@@ -729,6 +767,7 @@ cudaError_t launch_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
     a.w2s = p.w2s;
     a.h = reinterpret_cast<__nv_bfloat16*>(p.ws + L.h);
     a.y = reinterpret_cast<float*>(p.ws + L.y);
+    a.ssq = p.norm_w != nullptr ? reinterpret_cast<float*>(p.ws + L.ssq) : nullptr;
     a.tile_ready = reinterpret_cast<uint32_t*>(p.ws + L.tile_ready);
     a.d = s.d;
     a.I = s.I;

@@ -18,10 +18,10 @@ WsLayout ws_layout(const moe_shape& s) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(sizeof(StatusBlock));
-    // router partial logits: the K-range count is chosen for 152 SMs (GB300);
-    // another SM count only changes how the work is split
+    // router K-split (its cluster size): chosen for 152 SMs (GB300); another
+    // SM count only changes how the work is split
     L.router_kslices = router_kslices(s, 152);
-    L.logits = take((size_t)L.router_kslices * s.S * s.E * 4);
+    L.logits = take((size_t)s.S * s.E * 4);
     L.counts = take((size_t)s.E * 4);
     L.offsets = take((size_t)(s.E + 1) * 4);
     L.pos = take(P * 4);
@@ -32,6 +32,7 @@ WsLayout ws_layout(const moe_shape& s) {
     L.xg = take(P * s.d * 2);
     L.h = take(P * s.I * 2);
     L.y = take(P * s.d * 4);
+    L.ssq = take(P * (s.d / 128) * 4);                   // per-pick sums of y^2 by 128-row block
     L.xin = take((size_t)s.S * s.d * 2);                 // host-I/O staging
     L.hio_ids = take(P * 4);
     L.hio_w = take(P * 4);

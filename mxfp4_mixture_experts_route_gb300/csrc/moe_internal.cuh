@@ -36,12 +36,12 @@ struct Tile {
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, logits, counts, offsets, pos, src, tiles, active, tile_ready, xg, h, y;
+    size_t status, logits, counts, offsets, pos, src, tiles, active, tile_ready, xg, h, y, ssq;
     size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
     size_t total;
     int max_tiles;
     int max_picks;
-    int router_kslices;   // K-ranges of the router's partial logits
+    int router_kslices;   // K-ranges of the router (CTAs of one cluster)
 };
 
 WsLayout ws_layout(const moe_shape& s);

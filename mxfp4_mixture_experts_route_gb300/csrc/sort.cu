@@ -13,12 +13,10 @@ namespace moe {
 
 namespace {
 
-constexpr int SORT_THREADS = 1024;
-constexpr int SORT_WARPS = SORT_THREADS / 32;
 constexpr int MAX_K = 16;
 
-// One CTA.  Warp w owns the token range [w*tpw, (w+1)*tpw) (tpw a multiple of
-// 32) and walks it in groups of 32 tokens, lane = token.
+// One CTA of SORT_WARPS warps.  Warp w owns a range of 32-token groups and
+// walks it with lane = token.
 //   pass 1: validate ids, per-warp per-expert counts (smem)
 //   pass 2: per-expert exclusive scan over warps, scan over experts -> offsets,
 //           tile schedule, active list
@@ -26,20 +24,25 @@ constexpr int MAX_K = 16;
 //           the group that picked e (a 32-bit lane mask per expert)
 // Output: counts[E], offsets[E+1], pos[t*k+j] (-1 for an invalid pick),
 // src[p] = t*k+j, tiles[], active[], and n_picks / n_tiles / n_active.
-__global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict__ ids, int S, int E, int k,
-                                                       int32_t* __restrict__ counts,
-                                                       int32_t* __restrict__ offsets,
-                                                       int32_t* __restrict__ pos, int32_t* __restrict__ src,
-                                                       Tile* __restrict__ tiles, int32_t* __restrict__ active,
-                                                       uint32_t* __restrict__ tile_ready, int max_tiles,
-                                                       StatusBlock* __restrict__ sb) {
+// Global memory is only read for the ids (all of a token's ids in flight at
+// once); everything the passes share stays in shared memory.
+template <int SORT_WARPS>
+__global__ void __launch_bounds__(SORT_WARPS * 32) k_sort(const int32_t* __restrict__ ids, int S, int E, int k,
+                                                          int32_t* __restrict__ counts,
+                                                          int32_t* __restrict__ offsets,
+                                                          int32_t* __restrict__ pos, int32_t* __restrict__ src,
+                                                          Tile* __restrict__ tiles, int32_t* __restrict__ active,
+                                                          uint32_t* __restrict__ tile_ready, int max_tiles,
+                                                          StatusBlock* __restrict__ sb) {
+    constexpr int SORT_THREADS = SORT_WARPS * 32;
     extern __shared__ int32_t smem[];
     int32_t* cnt = smem;                        // [SORT_WARPS][E]
     uint32_t* mask = reinterpret_cast<uint32_t*>(smem + SORT_WARPS * E);  // [SORT_WARPS][E]
     int32_t* etot = smem + 2 * SORT_WARPS * E;  // [E] totals, then exclusive offsets
     int32_t* etil = etot + E;                   // [E] tiles per expert, then tile offsets
     int32_t* eact = etil + E;                   // [E] active flag, then active slot
-    __shared__ int32_t scan_tmp[SORT_THREADS / 32];
+    int32_t* ecnt = eact + E;                   // [E] picks per expert
+    __shared__ int32_t scan_tmp[32];
 
     const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
     for (int i = tid; i < 2 * SORT_WARPS * E; i += SORT_THREADS) smem[i] = 0;
@@ -50,23 +53,32 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
     const int gpw = (groups + SORT_WARPS - 1) / SORT_WARPS;   // groups per warp
     const int g0 = warp * gpw, g1 = min(groups, g0 + gpw);
 
+    // token t's k ids; bit j of the result is set when pick j is an id in
+    // [0, E) that no earlier pick of the token repeats
+    auto load_ids = [&](int t, int* my) -> uint32_t {
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) my[j] = (j < k) ? __ldg(ids + (size_t)t * k + j) : -1;
+        uint32_t valid = 0;
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
+            bool ok = j < k && my[j] >= 0 && my[j] < E;
+#pragma unroll
+            for (int q = 0; q < j; ++q) ok = ok && (my[q] != my[j]);
+            valid |= ok ? 1u << j : 0u;
+        }
+        return valid;
+    };
+
     // pass 1 ------------------------------------------------------------
     for (int g = g0; g < g1; ++g) {
         const int t = g * 32 + lane;
         if (t < S) {
             int my[MAX_K];
-            uint32_t valid = 0;
-            for (int j = 0; j < k; ++j) {
-                const int e = ids[(size_t)t * k + j];
-                my[j] = e;
-                bool ok = (e >= 0 && e < E);
-                for (int q = 0; q < j; ++q) ok = ok && (my[q] != e);
-                if (ok) {
-                    valid |= 1u << j;
-                    atomicAdd(&cnt[warp * E + e], 1);
-                } else {
-                    latch_status(sb, MOE_ERR_BAD_IDS, t * k + j);
-                }
+            const uint32_t valid = load_ids(t, my);
+#pragma unroll
+            for (int j = 0; j < MAX_K; ++j) {
+                if (valid >> j & 1u) atomicAdd(&cnt[warp * E + my[j]], 1);
+                else if (j < k) latch_status(sb, MOE_ERR_BAD_IDS, t * k + j);
             }
         }
     }
@@ -81,13 +93,18 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
             run += c;
         }
         etot[e] = run;
+        ecnt[e] = run;
         etil[e] = (run + NT - 1) / NT;
         eact[e] = run > 0 ? 1 : 0;
     }
     __syncthreads();
-    // three exclusive scans over E (E <= 512 < SORT_THREADS): one element per thread
+    // three exclusive scans over E (E <= 512): each thread scans a run of
+    // consecutive elements, then the runs' sums are scanned across the block
     auto block_scan = [&](int32_t* a, int32_t* total) {
-        const int v = tid < E ? a[tid] : 0;
+        const int per = (E + SORT_THREADS - 1) / SORT_THREADS;
+        const int b0 = tid * per, b1 = min(E, b0 + per);
+        int v = 0;
+        for (int i = b0; i < b1; ++i) v += a[i];
         int inc = v;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
@@ -97,28 +114,32 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
         if (lane == 31) scan_tmp[warp] = inc;
         __syncthreads();
         if (warp == 0) {
-            int w = scan_tmp[lane];
+            const int w = lane < SORT_WARPS ? scan_tmp[lane] : 0;
             int wi = w;
 #pragma unroll
             for (int m = 1; m < 32; m <<= 1) {
                 const int o = __shfl_up_sync(0xffffffffu, wi, m);
                 if (lane >= m) wi += o;
             }
-            scan_tmp[lane] = wi - w;   // exclusive prefix of warp sums
+            if (lane < SORT_WARPS) scan_tmp[lane] = wi - w;   // exclusive prefix of the warp sums
             if (lane == 31) *total = wi;
         }
         __syncthreads();
-        if (tid < E) a[tid] = scan_tmp[warp] + inc - v;
+        int run = scan_tmp[warp] + inc - v;
+        for (int i = b0; i < b1; ++i) {
+            const int x = a[i];
+            a[i] = run;
+            run += x;
+        }
         __syncthreads();
     };
     __shared__ int32_t tot_picks, tot_tiles, tot_active;
-    if (tid < E) counts[tid] = etot[tid];
-    __syncthreads();
+    for (int e = tid; e < E; e += SORT_THREADS) counts[e] = ecnt[e];
     block_scan(etot, &tot_picks);
     block_scan(etil, &tot_tiles);
     block_scan(eact, &tot_active);
     for (int e = tid; e < E; e += SORT_THREADS) {
-        const int n = counts[e];
+        const int n = ecnt[e];
         offsets[e] = etot[e];
         if (n > 0) active[eact[e]] = e;
         for (int i = 0, tb = etil[e]; i * NT < n; ++i) {
@@ -138,7 +159,6 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
         sb->work_next = 0;
         sb->work_next2 = 0;
     }
-    __syncthreads();
 
     // pass 3 ------------------------------------------------------------
     const uint32_t lt = (1u << lane) - 1u;
@@ -147,35 +167,31 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
         int my[MAX_K];
         uint32_t valid = 0;
         if (t < S) {
-            for (int j = 0; j < k; ++j) {
-                const int e = ids[(size_t)t * k + j];
-                my[j] = e;
-                bool ok = (e >= 0 && e < E);
-                for (int q = 0; q < j; ++q) ok = ok && (my[q] != e);
-                if (ok) {
-                    valid |= 1u << j;
-                    atomicOr(&mask[warp * E + e], 1u << lane);
-                } else {
-                    pos[(size_t)t * k + j] = -1;
-                }
+            valid = load_ids(t, my);
+#pragma unroll
+            for (int j = 0; j < MAX_K; ++j) {
+                if (valid >> j & 1u) atomicOr(&mask[warp * E + my[j]], 1u << lane);
+                else if (j < k) pos[(size_t)t * k + j] = -1;
             }
         }
         __syncwarp();
         int rank0[MAX_K];
-        for (int j = 0; j < k; ++j) {
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
             rank0[j] = -1;
             if (valid >> j & 1u) {
                 const int e = my[j];
                 const uint32_t m = mask[warp * E + e];
                 const int r = __popc(m & lt);
-                const int p = offsets[e] + cnt[warp * E + e] + r;
+                const int p = etot[e] + cnt[warp * E + e] + r;
                 pos[(size_t)t * k + j] = p;
                 src[p] = t * k + j;
                 rank0[j] = (r == 0) ? __popc(m) : -1;
             }
         }
         __syncwarp();
-        for (int j = 0; j < k; ++j) {
+#pragma unroll
+        for (int j = 0; j < MAX_K; ++j) {
             if (rank0[j] >= 0) {
                 const int e = my[j];
                 cnt[warp * E + e] += rank0[j];
@@ -195,8 +211,9 @@ __global__ void __launch_bounds__(128) k_gather(const __nv_bfloat16* __restrict_
                                                 __nv_bfloat16* __restrict__ xg,
                                                 const StatusBlock* __restrict__ sb) {
     const int p = blockIdx.x;
+    const int sp = src[p];                 // read beside n_picks: src has max_picks entries
     if (p >= sb->n_picks) return;
-    const int t = src[p] / k;
+    const int t = sp / k;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     uint4* o = reinterpret_cast<uint4*>(xg + (size_t)p * d);
     for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
@@ -215,11 +232,15 @@ __global__ void __launch_bounds__(128) k_gather(const __nv_bfloat16* __restrict_
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     char* ws = p.ws;
     StatusBlock* sb = reinterpret_cast<StatusBlock*>(ws + L.status);
-    const size_t smem = (size_t)(2 * SORT_WARPS * s.E + 3 * s.E) * sizeof(int32_t);
-    cudaError_t e = cudaFuncSetAttribute(k_sort, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    // small batches: 8 warps (the per-warp tables are then 8 x E); large: 32
+    const bool big = (size_t)s.S * s.k > 2048;
+    const int warps = big ? 32 : 8;
+    const size_t smem = (size_t)(2 * warps * s.E + 4 * s.E) * sizeof(int32_t);
+    auto kern = big ? k_sort<32> : k_sort<8>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     timing_begin(K_SORT, st);
-    k_sort<<<1, SORT_THREADS, smem, st>>>(p.ids, s.S, s.E, s.k, reinterpret_cast<int32_t*>(ws + L.counts),
+    kern<<<1, warps * 32, smem, st>>>(p.ids, s.S, s.E, s.k, reinterpret_cast<int32_t*>(ws + L.counts),
                                           reinterpret_cast<int32_t*>(ws + L.offsets),
                                           reinterpret_cast<int32_t*>(ws + L.pos),
                                           reinterpret_cast<int32_t*>(ws + L.src),
