@@ -8,8 +8,7 @@
  *     A      "router logits (fp32)"
  *     route  "every CTA routes every token (identical top-8)"; route_token:
  *            "sigmoid + ..." (the rest of that summary is cut off on the page)
- *     C, D   "gate_up / down of the local experts: MXFP4 weights ..., decoded
- *            in registers, bf16 MFMA"
+ *     C, D   "gate_up / down of the local experts: MXFP4 weights ..."
  *     E      "per-pick post-expert norm and weighted sum"
  *   vllm.models.muse_spark.amd.mono.kernels.k5, HA: "router (fp32 ...) ...
  *     top-8 ... h, top-k ids / weights for HM"
@@ -31,14 +30,21 @@
  * (sign, 2 exponent bits with bias 1, 1 mantissa bit); an e8m0 scale byte b
  * means 2^(b-127) and covers 32 consecutive K-elements of one row.  Packed
  * rows are row-major with K contiguous: byte j holds element 2j in its low
- * nibble and element 2j+1 in its high nibble.  Scale bytes 0..128 are
- * supported (block scales 2^-127 .. 2^1, so that every weight is exact in
- * bf16); a byte above 128 (255 is NaN in the MX format) latches
- * MOE_ERR_BAD_SCALE on the device and its block is read as zero.
+ * nibble and element 2j+1 in its high nibble.  Scale bytes 0..254 (block
+ * scales 2^-127 .. 2^127) are supported; the byte 255, NaN in the MX format,
+ * latches MOE_ERR_BAD_SCALE on the device (the affected outputs are NaN).
+ *
+ * Precision: the expert GEMMs run on the tensor core's block-scaled e2m1 x
+ * e4m3 path with fp32 accumulation.  The weights enter exactly; each bf16
+ * token row enters as two e4m3 rows (leading and trailing 4 significant
+ * bits) under a power-of-two scale per 32 elements, which is exact up to
+ * 2^-17 of the block's largest magnitude; h = silu(g) * u enters the same
+ * way from fp32 (about 9 significant bits, like a bf16 rounding).
  *
  * Conventions for every entry point:
  *   - All tensor pointers are DEVICE pointers (cudaMalloc'd or equivalent),
- *     16-byte aligned, owned by the caller, and must stay valid until the
+ *     16-byte aligned (the packed weights w13 and w2: 32-byte aligned),
+ *     owned by the caller, and must stay valid until the
  *     work queued on `stream` has finished.  Nothing is allocated, freed or
  *     cached by the library on these paths; it keeps no state between calls
  *     except per-device kernel attributes.
@@ -72,12 +78,12 @@ extern "C" {
 #define MOE_OK                     0
 #define MOE_ERR_INVALID_ARG       -1  /* NULL pointer, negative size, bad flags */
 #define MOE_ERR_UNSUPPORTED_SHAPE -2  /* shape outside the supported set (below) */
-#define MOE_ERR_ALIGNMENT         -3  /* a pointer is not 16-byte (ws: 256-byte) aligned */
+#define MOE_ERR_ALIGNMENT         -3  /* a pointer is not 16-byte (w13, w2: 32; ws: 256) aligned */
 #define MOE_ERR_WORKSPACE         -4  /* ws_bytes < moe_workspace_bytes() */
 #define MOE_ERR_CUDA              -5  /* a CUDA runtime call or launch failed */
 #define MOE_ERR_TIMEOUT           -6  /* device: a bounded wait ran out */
 #define MOE_ERR_BAD_IDS           -7  /* device: an expert id outside [0, E) */
-#define MOE_ERR_BAD_SCALE         -8  /* device: an e8m0 byte above 128 */
+#define MOE_ERR_BAD_SCALE         -8  /* device: an e8m0 scale byte of 255 (NaN) */
 #define MOE_ERR_NO_DEVICE         -9  /* current device is not sm_103 (GB300) */
 
 /* moe_shape.flags */

@@ -1,56 +1,54 @@
-// MXFP4 expert GEMMs on the 5th-generation tensor cores: one persistent kernel
-// runs every gate_up unit and then every down unit of the call.
+// MXFP4 expert GEMMs on the 5th-generation tensor cores with hardware block
+// scaling: one persistent kernel runs every gate_up unit and then every down
+// unit of the call.
 //
 // vllm.models.muse_spark.amd.mono.kernels.k3, stages C, D: "gate_up / down of
-// the local experts: MXFP4 weights ..., decoded in registers, bf16 MFMA";
-// fp4_mma: "Chunk c (256 K) of a 16-row MXFP4 group: 8 MFMA steps"; mx_chunk:
-// rows x K chunk of an MXFP4 weight and its e8m0 scales; task_ring: compute
-// the current task with the next tasks' loads in flight.
-// vllm.models.kimi_k3.amd.specialized_decode.mono.layer: the static weights
-// stream while earlier stages settle, weights issued before the first wait.
+// the local experts: MXFP4 weights ...": the weights stay in their MX form,
+// e2m1 codes with one e8m0 scale per 32 elements of a row; fp4_mma: a 256-K
+// chunk of a row group per step; task_ring: compute the current task with the
+// next tasks' loads in flight.  vllm.models.kimi_k3.amd.specialized_decode.
+// mono.layer: the static weights stream while earlier stages settle, weights
+// issued before the first wait.
 //
-// GB300 design (one persistent CTA per SM, 24 warps):
+// GB300 design.  The pages decode the e2m1 codes to 16-bit values in
+// registers for a bf16 MMA.  On sm_103a the tensor core takes e2m1 operands
+// and e8m0 block scales itself (tcgen05.mma kind::mxf8f6f4 block_scale), and
+// the TMA unpacks packed 4-bit codes into the tensor core's operand layout on
+// the way to shared memory, so no thread touches a weight byte.  The other
+// operand must then be an 8-bit float: each bf16 token row x (and each fp32 h
+// row) is written as two e4m3 rows, hi = e4m3(x / 2^s) and lo = e4m3(x / 2^s
+// - hi), with 2^s an e8m0 scale per 32 elements chosen so that the block's
+// largest magnitude lands in [128, 256).  hi carries the leading 4 significant
+// bits and lo the next 4, so hi + lo is x / 2^s exactly for a bf16 x (to
+// within 2^-17 of the block maximum for elements more than 2^9 below it).
+// The MMA's N = 32 columns are the hi and lo rows of a 16-pick tile; the
+// epilogue adds each pick's two columns.
+//
+// One persistent CTA per SM, 12 warps:
 //   warp 0      weight producer: per 256-K stage of a unit, the weight tile
-//               (128 rows x 256 K of packed e2m1, 16 KB; gate and up rows in
-//               one 4-D box) and its e8m0 bytes into a ring of weight stages,
-//               and an L2 prefetch of the weight tile PF stages ahead.  Under
-//               full load the HBM latency is several microseconds, more than
-//               the shared memory can cover at the bandwidth wanted; the L2
-//               prefetch keeps the rest of the bytes in flight.
-//   warp 7      token producer: the token tile (N picks x 256 K bf16, one 3-D
-//               box of four 128-byte-swizzled slabs) into a ring of its own;
-//               for a down unit it first waits (bounded) for the tile's h.
-//   warps 1-2   MMA issuers (lane 0 of each): tcgen05.mma kind::f16, M = 128,
-//               N = picks, K = 16, A = decoded weights in TMEM, B = token tile
-//               in shared memory.  Issuer m takes the 128-K sub-chunks q = m
-//               mod 2 of every unit into an fp32 accumulator of its own (double
-//               buffered); the epilogue sums the two.  One thread issues one
-//               MMA every ~50 cycles and each wait on an mbarrier drains its
-//               MMAs, so at N = 16 one issuer caps the tensor rate below what
-//               the weight stream needs; two issuers overlap.  Each TMEM A stage
-//               belongs to one issuer (stage q mod NA has the parity of q), so
-//               all uses of a stage complete in that issuer's order and no
-//               waiter is ever two phases ahead of an mbarrier.
-//   warps 8-23  decoders (groups of four warps; group g takes the 128-K
-//               sub-chunks g, g+G, ...): each thread owns one weight row, reads
-//               its 64 bytes (128 e2m1) and scale byte from shared memory
-//               (releasing the weight stage at once), turns them into bf16 with
-//               the block scale applied and stores them into a TMEM A stage.
-//   warps 3-6   epilogue: accumulators -> h = silu(g) * u (bf16) for gate_up,
-//               y (fp32) for down.
+//               (128 rows x 256 K e2m1 = 16 KB of HBM, 32 KB unpacked in
+//               shared memory; gate and up rows in one 4-D box) and its e8m0
+//               bytes into a ring of weight stages, and an L2 prefetch of the
+//               weight tile PF stages ahead (under full load the HBM latency
+//               is several microseconds, more than the shared memory covers at
+//               the bandwidth wanted).
+//   warp 7      token producer: the token tile (32 e4m3 rows x 256 K, one 3-D
+//               box of two 128-byte-swizzled slabs) and the tile's 16 rows of
+//               block scales (one bulk copy) into a ring of its own; for a
+//               down unit it first waits (bounded) for the tile's h.
+//   warps 8-11  scale movers: copy the stage's weight and token block scales
+//               from shared memory into TMEM, in the layout the MMA reads.
+//   warps 1-2   MMA issuers (lane 0 of each): M = 128 weight rows, N = 32,
+//               K = 32; issuer m takes the 128-K half m of every stage into an
+//               fp32 accumulator of its own (double buffered by unit).
+//   warps 3-6   epilogue: the issuers' accumulators and each pick's hi and lo
+//               column added; h = silu(g) * u split into e4m3 hi/lo rows with a
+//               block scale per 32 rows for gate_up; y (fp32) and per-128-row
+//               sums of squares for down.
 // Work units, in a static round-robin over the CTAs: gate_up units first
 // (64 gate rows stacked on the matching 64 up rows = one M = 128 operand), then
 // down units (128 rows of w2).  A down unit needs the h rows of its tile: the
 // counter of the tile, which every finished gate_up unit of it increments.
-//
-// Decode: an e2m1 code (s, e1, e0, m) is placed in a bf16 as sign bit 15 and
-// bits 8..6 = (e1, e0, m): that bf16 equals the e2m1 value times 2^-126
-// (exact, subnormal for e = 0), so one bf16x2 multiply by 2^(b - 1) applies
-// the e8m0 scale 2^(b - 127) exactly for b in 0..128.  Two codes 16 bits apart
-// in a 32-bit word share one integer multiply (x 0x1040 or x 0x104) and one
-// mask.  The K order inside every group of 8 elements is therefore
-// (0, 4, 1, 5, 2, 6, 3, 7); the gathered tokens and h are stored in the same
-// order, so the MMA sums matching pairs.
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -60,61 +58,59 @@ namespace moe {
 
 namespace {
 
-constexpr int KC = 128;                      // K elements of one decode sub-chunk (one TMEM A stage)
-constexpr int KS = 256;                      // K elements of one shared-memory stage (two sub-chunks)
+constexpr int KS = 256;                      // K elements of one stage
 constexpr int AROWS = 128;                   // MMA M
-constexpr int A_SUB = AROWS * KC / 2;        // packed e2m1 of one sub-chunk: 8 KB
-constexpr int A_BYTES = 2 * A_SUB;           // of one stage: 16 KB
-#ifndef MOE_TC_TOKEN_STAGES
-#define MOE_TC_TOKEN_STAGES 4
+constexpr int NB = 2 * NT;                   // MMA N: a hi and a lo row per pick
+constexpr int A_SLAB = AROWS * 128;          // one 128-K slab of the weight tile in shared memory (unpacked)
+constexpr int A_SMEM = 2 * A_SLAB;           // 32 KB
+constexpr int A_TX = AROWS * KS / 2;         // packed bytes of a weight tile: the TMA transaction count
+constexpr int B_SLAB = NB * 128;             // one 128-K slab of the token tile
+constexpr int B_SMEM = 2 * B_SLAB;           // 8 KB
+constexpr int BS_BYTES = NT * TOKEN_SCALE_ROW;   // the tile's token scale rows
+#ifndef MOE_MX_TOKEN_STAGES
+#define MOE_MX_TOKEN_STAGES 4
 #endif
-#ifndef MOE_TC_DEC_GROUPS
-#define MOE_TC_DEC_GROUPS 4
+#ifndef MOE_MX_PREFETCH
+#define MOE_MX_PREFETCH 16
 #endif
-#ifndef MOE_TC_PREFETCH
-#define MOE_TC_PREFETCH 16
-#endif
-constexpr int NSB = MOE_TC_TOKEN_STAGES;       // token-tile stages
-constexpr int DEC_GROUPS = MOE_TC_DEC_GROUPS;  // decoder groups of 4 warps
-constexpr int PF = MOE_TC_PREFETCH;            // L2 prefetch distance in weight stages
-constexpr int A_COLS = KC / 2;               // TMEM columns of one A stage
+constexpr int NSB = MOE_MX_TOKEN_STAGES;     // token-tile stages
+constexpr int PF = MOE_MX_PREFETCH;          // L2 prefetch distance in weight stages
 constexpr int TMEM_COLS = 512;
 constexpr int NMMA = 2;                      // MMA-issuing warps (one thread each)
-constexpr int MMA_WARP0 = 1, EPI_WARP0 = 3, TOK_WARP = 7, DEC_WARP0 = 8;
-static_assert(MOE_TC_DEC_GROUPS % NMMA == 0, "decoder group g feeds issuer g mod NMMA");
-constexpr int NUM_WARPS = DEC_WARP0 + 4 * DEC_GROUPS;
+constexpr int SF_COL0 = 2 * NMMA * NB;       // TMEM columns of the scale slots (after the accumulators)
+// One stage's scale slot in TMEM, 64 columns: the weight scales of K steps
+// 0-3 at +0 and of K steps 4-7 at +16 (row m of the tile in lane m, column
+// + m / 32), the token scales at +32 and +48 (column n in lane n of every lane
+// quarter).  Every scale address the MMA gets is a multiple of 16 columns.
+constexpr int SF_SLOT = 64;
+constexpr int SF_A1 = 16, SF_B0 = 32, SF_B1 = 48;
+constexpr int MMA_WARP0 = 1, EPI_WARP0 = 3, TOK_WARP = 7, SF_WARP0 = 8;
+constexpr int NUM_WARPS = 12;
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 constexpr int UR = 32;                       // unit ring entries
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 
-// STMA: the e8m0 bytes come by TMA, 16 bytes (512 K) of each row per stage,
-// when the scale rows are 16-byte aligned (K % 512 == 0); otherwise by 4-byte
-// cp.async, 8 bytes (256 K) of each row per stage.
-template <int N, bool STMA>
+// STMA: the e8m0 bytes of the weights come by TMA, 16 bytes (512 K) of each
+// row per stage, when the scale rows are 16-byte aligned (K % 512 == 0);
+// otherwise by 4-byte cp.async, 8 bytes (256 K) of each row per stage.
+template <bool STMA>
 struct Cfg {
-    static constexpr int B_BOX = N * 128;                      // N rows x 64 bf16 (one slab)
-    static constexpr int B_BYTES = 4 * B_BOX;                  // token tile of a stage (256 K)
     static constexpr int SC_ROW = STMA ? 16 : 8;               // e8m0 bytes of a row in a stage
     static constexpr int SC_BYTES = AROWS * SC_ROW;
-    static constexpr int SC_OFF = A_BYTES;                     // within a weight stage
-    static constexpr int A_STAGE = ((A_BYTES + SC_BYTES) + 1023) / 1024 * 1024;
-    static constexpr int B_STAGE = (B_BYTES + 1023) / 1024 * 1024;
-    static constexpr int XCH_STRIDE = N + 1;
+    static constexpr int SC_OFF = A_SMEM;                      // within a weight stage
+    static constexpr int A_STAGE = (A_SMEM + SC_BYTES + 1023) / 1024 * 1024;
+    static constexpr int B_STAGE = (B_SMEM + BS_BYTES + 1023) / 1024 * 1024;
+    static constexpr int XCH_STRIDE = NT + 1;
     static constexpr int XCH_BYTES = 64 * XCH_STRIDE * 4;
     static constexpr int RING_BYTES = UR * 32;
     static constexpr int MISC = 1024 /*align slack*/ + XCH_BYTES + RING_BYTES + 1024 /*barriers*/;
-    // weight stages: an even count, so that each stage's two sub-chunks always
-    // go to the same two decoder groups (no group is ever two phases ahead)
-    static constexpr int NSA = (232448 - MISC - NSB * B_STAGE) / A_STAGE / 2 * 2;
+    static constexpr int NSA_FIT = (232448 - MISC - NSB * B_STAGE) / A_STAGE;
+    static constexpr int NSA_TMEM = (TMEM_COLS - SF_COL0) / SF_SLOT;
+    static constexpr int NSA = NSA_FIT < NSA_TMEM ? NSA_FIT : NSA_TMEM;
     static constexpr int SMEM = MISC + NSB * B_STAGE + NSA * A_STAGE;
-    // TMEM: 2 buffers x NMMA fp32 accumulators of N columns, then as many A
-    // stages as fit
-    static constexpr int A_COL0 = (2 * NMMA * N + 63) / 64 * 64;
-    static constexpr int NA = (TMEM_COLS - A_COL0) / A_COLS / NMMA * NMMA;   // a multiple of NMMA
-    static_assert(N % 16 == 0 && N >= 16 && N <= 64, "MMA N");
-    static_assert(NA >= 2 * NMMA && NA % NMMA == 0, "TMEM A stages: two or more per issuer");
-    static_assert(NSA >= 4 && (2 * NSA) % DEC_GROUPS == 0, "weight stages");
+    static_assert(NSA >= 3, "weight stages");
     static_assert(SMEM <= 232448, "shared memory per CTA");
+    static_assert(SF_COL0 + NSA * SF_SLOT <= TMEM_COLS, "TMEM columns");
 };
 
 struct Args {
@@ -122,18 +118,20 @@ struct Args {
     StatusBlock* sb;
     const uint8_t* w13s;
     const uint8_t* w2s;
-    __nv_bfloat16* h;
+    uint8_t* hq;          // [2P][I] e4m3: row 2p = hi, row 2p + 1 = lo of pick p's h
+    uint8_t* hs;          // [ceil(I/256)][P + NT][16] e8m0 block scales of h
     float* y;
-    float* ssq;      // per-pick sums of y^2 by 128-row block, or null
+    float* ssq;           // per-pick sums of y^2 by 128-row block, or null
     uint32_t* tile_ready;
-    int d, I;
+    const uint8_t* xs;    // [ceil(d/256)][P + NT][16] e8m0 block scales of the gathered tokens
+    int d, I, P;
 };
 
 struct Unit {
     int down;        // 0: gate_up, 1: down
     int tile, mb;    // tile index and row block
     int e, p0, n;
-    int stages;      // shared-memory stages (256 K each) of the unit
+    int stages;      // 256-K stages of the unit
     int pad;
 };
 
@@ -161,49 +159,14 @@ __device__ __forceinline__ int weight_row(const Unit& U, int r, const Args& a) {
     return U.e * a.d + U.mb * AROWS + r;
 }
 
-// e2m1 x 32 (16 bytes) + e8m0 byte -> 16 bf16x2 words in MMA K order
-__device__ __forceinline__ void decode_block(const uint4 q, uint32_t sbyte, uint32_t* out, StatusBlock* sb) {
-    uint32_t mult;
-    if (sbyte <= 128u) {
-        mult = (sbyte + 126u) << 7;          // bf16 bits of 2^(b - 1)
-    } else {
-        latch_status(sb, MOE_ERR_BAD_SCALE, (int)sbyte);
-        mult = 0u;
-    }
-    mult |= mult << 16;
-    const __nv_bfloat162 m2 = *reinterpret_cast<const __nv_bfloat162*>(&mult);
-    const uint32_t w[4] = {q.x, q.y, q.z, q.w};
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-        const uint32_t x = w[i], x8 = x >> 8;
-        uint32_t o[4];
-        o[0] = ((x & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;    // codes 0 and 4 of the word
-        o[1] = ((x & 0x00F000F0u) * 0x104u) & 0x81C081C0u;     // codes 1 and 5
-        o[2] = ((x8 & 0x000F000Fu) * 0x1040u) & 0x81C081C0u;   // codes 2 and 6
-        o[3] = ((x8 & 0x00F000F0u) * 0x104u) & 0x81C081C0u;   // codes 3 and 7
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            __nv_bfloat162 v = *reinterpret_cast<const __nv_bfloat162*>(&o[j]);
-            v = __hmul2(v, m2);
-            out[4 * i + j] = *reinterpret_cast<const uint32_t*>(&v);
-        }
-    }
-}
-
-// position of K-element i in the MMA order of its group of 8
-__device__ __forceinline__ int kperm(int i) {
-    const int e = i & 7;
-    return (i & ~7) | (e < 4 ? 2 * e : 2 * (e - 4) + 1);
-}
-
-template <int N, bool STMA>
+template <bool STMA>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
-    k_experts_tc(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
-                 const __grid_constant__ CUtensorMap tm_xg, const __grid_constant__ CUtensorMap tm_h,
+    k_experts_mx(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
+                 const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_hq,
                  const __grid_constant__ CUtensorMap tm_w13s, const __grid_constant__ CUtensorMap tm_w2s,
                  const Args a) {
-    using C = Cfg<N, STMA>;
-    constexpr int NSA = C::NSA, NA = C::NA, A_COL0 = C::A_COL0;
+    using C = Cfg<STMA>;
+    constexpr int NSA = C::NSA;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* wst = smem;                                  // weight stages [NSA][A_STAGE]
@@ -211,13 +174,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     float* xch = reinterpret_cast<float*>(tst + NSB * C::B_STAGE);
     Unit* uring = reinterpret_cast<Unit*>(reinterpret_cast<uint8_t*>(xch) + C::XCH_BYTES);
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(uring) + C::RING_BYTES);
-    uint64_t* full_a = bars;                // [NSA]
-    uint64_t* empty_a = full_a + NSA;       // [NSA]
-    uint64_t* full_b = empty_a + NSA;       // [NSB]
-    uint64_t* empty_b = full_b + NSB;       // [NSB]
-    uint64_t* a_full = empty_b + NSB;       // [NA]
-    uint64_t* a_empty = a_full + NA;        // [NA]
-    uint64_t* acc_full = a_empty + NA;      // [2]
+    uint64_t* full_a = bars;                // [NSA] weight tile + its scales landed
+    uint64_t* empty_a = full_a + NSA;       // [NSA] both issuers done with the weight stage
+    uint64_t* full_b = empty_a + NSA;       // [NSB] token tile + its scales landed
+    uint64_t* empty_b = full_b + NSB;       // [NSB] both issuers done with the token stage
+    uint64_t* sf_full = empty_b + NSB;      // [NSA] the stage's scales are in TMEM
+    uint64_t* acc_full = sf_full + NSA;     // [2]
     uint64_t* acc_empty = acc_full + 2;     // [2]
     uint64_t* u_full = acc_empty + 2;       // [UR]
     uint64_t* u_empty = u_full + UR;        // [UR]
@@ -232,15 +194,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSA; ++i) {
             ptx::mbar_init(&full_a[i], STMA ? 1 : 1 + 32);   // expect_tx (+ 32 cp.async arrivals)
-            ptx::mbar_init(&empty_a[i], 2 * 4);             // the 4 decoder warps of each sub-chunk
+            ptx::mbar_init(&empty_a[i], NMMA);
+            ptx::mbar_init(&sf_full[i], 4);                 // the four scale movers
         }
         for (int i = 0; i < NSB; ++i) {
             ptx::mbar_init(&full_b[i], 1);
-            ptx::mbar_init(&empty_b[i], 2);                 // MMA commits of the stage's two sub-chunks
-        }
-        for (int i = 0; i < NA; ++i) {
-            ptx::mbar_init(&a_full[i], 4);
-            ptx::mbar_init(&a_empty[i], 1);
+            ptx::mbar_init(&empty_b[i], NMMA);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&acc_full[i], NMMA);
@@ -248,7 +207,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
         for (int i = 0; i < UR; ++i) {
             ptx::mbar_init(&u_full[i], 1);
-            ptx::mbar_init(&u_empty[i], NMMA + 1 + 4 * DEC_GROUPS + 4);   // MMA, token producer, decoders, epilogue
+            ptx::mbar_init(&u_empty[i], NMMA + 1 + 4 + 4);   // MMA, token producer, scale movers, epilogue
         }
         for (int i = 0; i < NMMA; ++i) ptx::mbar_init(&fin[i], 1);
         *abort_flag = 0;
@@ -264,8 +223,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     }
     if (warp == TOK_WARP && lane == 0) {
-        ptx::prefetch_tensormap(&tm_xg);
-        ptx::prefetch_tensormap(&tm_h);
+        ptx::prefetch_tensormap(&tm_xq);
+        ptx::prefetch_tensormap(&tm_hq);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -379,7 +338,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 uint8_t* st = wst + s * C::A_STAGE;
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&full_a[s], A_BYTES + (STMA ? C::SC_BYTES : 0));
+                    ptx::mbar_arrive_expect_tx(&full_a[s], A_TX + (STMA ? C::SC_BYTES : 0));
                     if (!U.down) {
                         // gate rows mb*64.. and up rows I + mb*64.. of expert e, 2 slabs of 128 K
                         ptx::tma_load_4d(st, &tm_w13, 0, r0, 2 * U.e, 2 * c, &full_a[s], pol_w);
@@ -391,8 +350,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!STMA) {
                     // e8m0 bytes of this stage: rows lane, lane+32, lane+64, lane+96, 4 bytes a
-                    // sub-chunk; a sub-chunk past K (odd K/128) reads the row's first bytes
-                    // (its weights are zero-filled, so they are multiplied by zero)
+                    // 128-K half; a half past K (odd K/128) reads the row's first bytes (its
+                    // codes are zero-filled, so they are multiplied by zero)
                     const uint8_t* sbase = U.down ? a.w2s : a.w13s;
                     const int kb = K / 32;
 #pragma unroll
@@ -415,6 +374,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == TOK_WARP) {
         // ------------------------------------------------------------ token producer
         const uint64_t pol_x = ptx::policy_evict_last();
+        const size_t tab_rows = (size_t)a.P + NT;
         int ts = 0;
         bool ok = true;
         for (int i = 0; i < my_units && ok; ++i) {
@@ -423,7 +383,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (lane == 0) fail(12);
                 break;
             }
-            const CUtensorMap* tmB = U.down ? &tm_h : &tm_xg;
+            const CUtensorMap* tmB = U.down ? &tm_hq : &tm_xq;
+            const uint8_t* tab = U.down ? a.hs : a.xs;
             if (U.down) {
                 // the tile's h rows: complete once all its gate_up units are done
                 uint32_t ready = 0;
@@ -451,18 +412,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 if (lane == 0) {
-                    ptx::mbar_arrive_expect_tx(&full_b[s], C::B_BYTES);
-                    ptx::tma_load_3d(tst + s * C::B_STAGE, tmB, 0, U.p0, 4 * c, &full_b[s], pol_x);
+                    uint8_t* st = tst + s * C::B_STAGE;
+                    ptx::mbar_arrive_expect_tx(&full_b[s], B_SMEM + BS_BYTES);
+                    ptx::tma_load_3d(st, tmB, 0, 2 * U.p0, 2 * c, &full_b[s], pol_x);
+                    ptx::bulk_load(st + B_SMEM, tab + ((size_t)c * tab_rows + U.p0) * TOKEN_SCALE_ROW, BS_BYTES,
+                                   &full_b[s], pol_x);
                 }
                 __syncwarp();
             }
         }
+    } else if (warp >= SF_WARP0) {
+        // ------------------------------------------------------------ scale movers
+        const int q = warp - SF_WARP0;    // TMEM lane quarter of this warp
+        const int r = 32 * q + lane;      // weight row of this thread
+        const uint32_t lane_base = (uint32_t)(32 * q) << 16;
+        int ts = 0;
+        bool ok = true;
+        for (int i = 0; i < my_units && ok; ++i) {
+            Unit U;
+            if (!take_unit(i, U)) {
+                if (lane == 0) fail(10);
+                break;
+            }
+            for (int c = 0; c < U.stages; ++c, ++ts) {
+                const int s = ts % NSA, sbi = ts % NSB;
+                if (!ptx::mbar_wait_warp(&full_a[s], (ts / NSA) & 1, abort_flag, WAIT_NS) ||
+                    !ptx::mbar_wait_warp(&full_b[sbi], (ts / NSB) & 1, abort_flag, WAIT_NS)) {
+                    if (lane == 0) fail(5);
+                    ok = false;
+                    break;
+                }
+                const uint8_t* st = wst + s * C::A_STAGE;
+                const uint2 wa = *reinterpret_cast<const uint2*>(st + C::SC_OFF + C::SC_ROW * r + (STMA ? 8 * (c & 1) : 0));
+                const uint2 wb = *reinterpret_cast<const uint2*>(tst + sbi * C::B_STAGE + B_SMEM + TOKEN_SCALE_ROW * (lane >> 1));
+                // 0xFF is NaN in e8m0
+                const uint32_t nan_a = __vcmpeq4(wa.x, 0xFFFFFFFFu) | __vcmpeq4(wa.y, 0xFFFFFFFFu);
+                if (nan_a) latch_status(sb, MOE_ERR_BAD_SCALE, 255);
+                const uint32_t col = SF_COL0 + s * SF_SLOT;
+                // row r = 32q + lane is read at column col + q (K steps 0-3) and
+                // col + SF_A1 + q (K steps 4-7); the warp writes its word into all
+                // four columns of a group (aligned stores): the other lane quarters'
+                // columns of these lanes are never read
+                ptx::tmem_st4_rep(tmem + lane_base + col, wa.x);
+                ptx::tmem_st4_rep(tmem + lane_base + col + SF_A1, wa.y);
+                // token column n = lane (pick lane / 2, hi or lo row), in every lane quarter
+                ptx::tmem_st4_rep(tmem + lane_base + col + SF_B0, wb.x);
+                ptx::tmem_st4_rep(tmem + lane_base + col + SF_B1, wb.y);
+                ptx::tmem_st_wait();
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&sf_full[s]);
+            }
+        }
     } else if (warp >= MMA_WARP0 && warp < MMA_WARP0 + NMMA) {
         // ------------------------------------------------------------ MMA issuers
-        constexpr uint32_t idesc = ptx::idesc_bf16_f32(AROWS, N);
-        const int m = warp - MMA_WARP0;   // this issuer takes sub-chunks q = m mod NMMA (every unit
-                                          // has an even number of sub-chunks, so it gets at least one)
-        int q = 0;                        // sub-chunk sequence number
+        const int m = warp - MMA_WARP0;   // this issuer takes the 128-K half m of every stage
+        int ts = 0;
         for (int i = 0; i < my_units; ++i) {
             Unit U;
             if (!take_unit(i, U)) {
@@ -472,37 +477,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             if (lane == 0) {
                 const int ab = i & 1;
-                const uint32_t d_tmem = tmem + (ab * NMMA + m) * N;
-                bool first = true;
-                for (int cc = 0; cc < 2 * U.stages && ok; ++cc, ++q) {
-                    if (q % NMMA != m) continue;
-                    if (first && !ptx::mbar_wait(&acc_empty[ab], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
+                const uint32_t d_tmem = tmem + (ab * NMMA + m) * NB;
+                for (int c = 0; c < U.stages && ok; ++c, ++ts) {
+                    const int s = ts % NSA, sbi = ts % NSB;
+                    if (c == 0 && !ptx::mbar_wait(&acc_empty[ab], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
                         fail(3);
                         ok = false;
                         break;
                     }
-                    const int ts = q >> 1, sbi = ts % NSB, as = q % NA, hh = q & 1;
-                    if (!ptx::mbar_wait(&full_b[sbi], (ts / NSB) & 1, abort_flag, WAIT_NS) ||
-                        !ptx::mbar_wait(&a_full[as], (q / NA) & 1, abort_flag, WAIT_NS)) {
+                    if (!ptx::mbar_wait(&full_a[s], (ts / NSA) & 1, abort_flag, WAIT_NS) ||
+                        !ptx::mbar_wait(&full_b[sbi], (ts / NSB) & 1, abort_flag, WAIT_NS) ||
+                        !ptx::mbar_wait(&sf_full[s], (ts / NSA) & 1, abort_flag, WAIT_NS)) {
                         fail(4);
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t b0 = ptx::smem_u32(tst + sbi * C::B_STAGE + 2 * hh * C::B_BOX);
-                    const uint32_t a0 = tmem + A_COL0 + as * A_COLS;
+                    const uint32_t a0 = ptx::smem_u32(wst + s * C::A_STAGE) + m * A_SLAB;
+                    const uint32_t b0 = ptx::smem_u32(tst + sbi * C::B_STAGE) + m * B_SLAB;
+                    const uint32_t col = SF_COL0 + s * SF_SLOT;
 #pragma unroll
-                    for (int kk = 0; kk < KC / 16; ++kk) {
-                        const uint64_t bd = ptx::smem_desc_sw128(b0 + (kk >> 2) * C::B_BOX + (kk & 3) * 32);
-                        ptx::mma_bf16_ts(d_tmem, a0 + kk * 8, bd, idesc, (!first || kk) ? 1u : 0u);
+                    for (int j = 0; j < 4; ++j) {
+                        ptx::mma_mx_ss(d_tmem, ptx::smem_desc_sw128(a0 + 32 * j), ptx::smem_desc_sw128(b0 + 32 * j),
+                                       ptx::idesc_mx_e2m1_e4m3(AROWS, NB, j, j), (c > 0 || j > 0) ? 1u : 0u,
+                                       tmem + col + SF_A1 * m, tmem + col + SF_B0 + (SF_B1 - SF_B0) * m);
                     }
-                    first = false;
-                    ptx::mma_commit(&a_empty[as]);
+                    ptx::mma_commit(&empty_a[s]);
                     ptx::mma_commit(&empty_b[sbi]);
                 }
                 if (ok) ptx::mma_commit(&acc_full[ab]);
             }
-            q = __shfl_sync(0xffffffffu, q, 0);
+            ts = __shfl_sync(0xffffffffu, ts, 0);
             if (!__shfl_sync(0xffffffffu, ok ? 1 : 0, 0)) break;
         }
         if (lane == 0) {
@@ -511,63 +516,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_wait(&fin[m], 0, abort_flag, WAIT_NS);
         }
         __syncwarp();
-    } else if (warp >= DEC_WARP0) {
-        // ------------------------------------------------------------ decoders
-        const int dw = warp - DEC_WARP0;
-        const int g = dw >> 2;            // this group takes sub-chunks g mod DEC_GROUPS
-        const int qd = warp & 3;          // TMEM lane quarter of this warp
-        const int r = 32 * qd + lane;     // weight row of this thread
-        const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-        int q = 0;
-        bool ok = true;
-        for (int i = 0; i < my_units && ok; ++i) {
-            Unit U;
-            if (!take_unit(i, U)) {
-                if (lane == 0) fail(10);
-                break;
-            }
-            for (int cc = 0; cc < 2 * U.stages; ++cc, ++q) {
-                if (q % DEC_GROUPS != g) continue;
-                const int ts = q >> 1, s = ts % NSA, as = q % NA, hh = q & 1;
-                if (!ptx::mbar_wait_warp(&full_a[s], (ts / NSA) & 1, abort_flag, WAIT_NS)) {
-                    if (lane == 0) fail(5);
-                    ok = false;
-                    break;
-                }
-                const uint8_t* st = wst + s * C::A_STAGE;
-                const uint8_t* arow = st + hh * A_SUB + r * 64;
-                uint4 w4[4];
-#pragma unroll
-                for (int j = 0; j < 4; ++j)
-                    w4[j] = *reinterpret_cast<const uint4*>(arow + ((j ^ ((r >> 1) & 3)) << 4));
-                const uint32_t sc = *reinterpret_cast<const uint32_t*>(
-                    st + C::SC_OFF + C::SC_ROW * r + (STMA ? 4 * (cc & 3) : 4 * hh));
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&empty_a[s]);
-                if (!ptx::mbar_wait_warp(&a_empty[as], ((q / NA) & 1) ^ 1, abort_flag, WAIT_NS)) {
-                    if (lane == 0) fail(6);
-                    ok = false;
-                    break;
-                }
-                ptx::tc_fence_after();
-                const uint32_t ta = tmem + lane_base + A_COL0 + as * A_COLS;
-#pragma unroll
-                for (int j = 0; j < 4; ++j) {
-                    uint32_t v[16];
-                    decode_block(w4[j], (sc >> (8 * j)) & 0xFFu, v, sb);
-                    ptx::tmem_st16(ta + 16 * j, v);
-                }
-                ptx::tmem_st_wait();
-                ptx::tc_fence_before();
-                __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&a_full[as]);
-            }
-        }
     } else {
         // ------------------------------------------------------------ epilogue
         const int qd = warp & 3;
         const int r = 32 * qd + lane;
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
+        const size_t tab_rows = (size_t)a.P + NT;
         for (int i = 0; i < my_units; ++i) {
             const int ab = i & 1;
             // the four epilogue warps take one decision before their named
@@ -582,19 +536,19 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::named_bar_sync(1, 128);
             if (*epi_flag) break;
             ptx::tc_fence_after();
-            // sum the issuers' accumulators (each issuer had sub-chunks of the unit)
-            float v[N];
+            // v[n]: both issuers' halves of K, hi + lo column of pick n
+            float v[NT];
 #pragma unroll
-            for (int n = 0; n < N; ++n) v[n] = 0.f;
+            for (int n = 0; n < NT; ++n) v[n] = 0.f;
 #pragma unroll
             for (int mm = 0; mm < NMMA; ++mm) {
-                uint32_t t[N];
+                uint32_t t[NB];
 #pragma unroll
-                for (int j = 0; j < N / 16; ++j)
-                    ptx::tmem_ld16(tmem + lane_base + (ab * NMMA + mm) * N + 16 * j, t + 16 * j);
+                for (int j = 0; j < NB / 16; ++j)
+                    ptx::tmem_ld16(tmem + lane_base + (ab * NMMA + mm) * NB + 16 * j, t + 16 * j);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int n = 0; n < N; ++n) v[n] += __uint_as_float(t[n]);
+                for (int n = 0; n < NT; ++n) v[n] += __uint_as_float(t[2 * n]) + __uint_as_float(t[2 * n + 1]);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -603,19 +557,46 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // lanes 0..63: gate of rows mb*64 + r; lanes 64..127: up of the same rows
                 if (r >= 64) {
 #pragma unroll
-                    for (int n = 0; n < N; ++n) xch[(r - 64) * C::XCH_STRIDE + n] = v[n];
+                    for (int n = 0; n < NT; ++n) xch[(r - 64) * C::XCH_STRIDE + n] = v[n];
                 }
                 ptx::named_bar_sync(1, 128);
                 if (r < 64) {
+                    // warp qd (0 or 1) holds the 32 rows of h block mb*2 + qd
                     const int ii = U.mb * 64 + r;
-                    const int col = kperm(ii);
+                    const int blk = ii / 32;
+                    float h[NT];
 #pragma unroll
-                    for (int n = 0; n < N; ++n) {
-                        if (n < U.n) {
-                            const float gv = v[n];
-                            const float uv = xch[r * C::XCH_STRIDE + n];
-                            const float hv = gv / (1.0f + __expf(-gv)) * uv;
-                            a.h[(size_t)(U.p0 + n) * a.I + col] = __float2bfloat16_rn(hv);
+                    for (int n = 0; n < NT; ++n) {
+                        const float gv = v[n];
+                        const float uv = xch[r * C::XCH_STRIDE + n];
+                        h[n] = n < U.n ? gv / (1.0f + __expf(-gv)) * uv : 0.f;
+                    }
+#pragma unroll
+                    for (int n = 0; n < NT; n += 2) {
+                        uint32_t byte2[2];
+                        float hs2[2];
+#pragma unroll
+                        for (int z = 0; z < 2; ++z) {
+                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[n + z])));
+                            int e = (int)((amax >> 23) & 0xFFu) - 7;
+                            e = e < 1 ? 1 : (e > 247 ? 247 : e);
+                            byte2[z] = (uint32_t)e;
+                            hs2[z] = h[n + z] * __uint_as_float((uint32_t)(254 - e) << 23);   // h / 2^(e - 127)
+                        }
+                        const uint32_t hi2 = ptx::cvt_e4m3x2(hs2[0], hs2[1]);
+                        float f0, f1;
+                        ptx::e4m3x2_to_f32(hi2, f0, f1);
+                        const uint32_t lo2 = ptx::cvt_e4m3x2(hs2[0] - f0, hs2[1] - f1);
+#pragma unroll
+                        for (int z = 0; z < 2; ++z) {
+                            if (n + z < U.n) {
+                                const size_t p = (size_t)(U.p0 + n + z);
+                                a.hq[(2 * p) * a.I + ii] = (uint8_t)(hi2 >> (8 * z));
+                                a.hq[(2 * p + 1) * a.I + ii] = (uint8_t)(lo2 >> (8 * z));
+                                if (lane == 0)
+                                    a.hs[((size_t)(blk >> 3) * tab_rows + p) * TOKEN_SCALE_ROW + (blk & 7)] =
+                                        (uint8_t)byte2[z];
+                            }
                         }
                     }
                     ptx::fence_proxy_async_global();
@@ -628,20 +609,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
                 const int m = U.mb * AROWS + r;
 #pragma unroll
-                for (int n = 0; n < N; ++n)
+                for (int n = 0; n < NT; ++n)
                     if (n < U.n) a.y[(size_t)(U.p0 + n) * a.d + m] = v[n];
                 if (a.ssq != nullptr) {
                     // sum of y^2 over the unit's 128 rows for every pick: a
-                    // reduce-scatter across the warp (lane l ends with picks
-                    // [idx, idx + c)), then the four warps' sums in warp order
-                    float q[N];
+                    // reduce-scatter across the warp (lane l ends with pick idx),
+                    // then the four warps' sums in warp order
+                    float q[NT];
 #pragma unroll
-                    for (int n = 0; n < N; ++n) q[n] = v[n] * v[n];
+                    for (int n = 0; n < NT; ++n) q[n] = v[n] * v[n];
                     int idx = 0;
 #pragma unroll
                     for (int step = 0; step < 5; ++step) {
                         const int o = 16 >> step;
-                        const int c = N >> step;        // values a lane holds before this step
+                        const int c = NT >> step;       // values a lane holds before this step
                         const bool hi = (lane & o) != 0;
                         if (c > 1) {
 #pragma unroll
@@ -655,17 +636,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             q[0] += __shfl_xor_sync(0xffffffffu, q[0], o);
                         }
                     }
-                    constexpr int C_END = N >= 32 ? N / 32 : 1;   // values a lane holds at the end
-                    constexpr int SHARE = 32 * C_END / N;          // lanes holding the same values
-                    float* part = xch;                             // [4][N]
-                    if (lane % SHARE == 0) {
-#pragma unroll
-                        for (int j = 0; j < C_END; ++j) part[qd * N + idx + j] = q[j];
-                    }
+                    static_assert(NT == 16, "the reduce-scatter leaves one pick on every lane pair");
+                    float* part = xch;                             // [4][NT]
+                    if ((lane & 1) == 0) part[qd * NT + idx] = q[0];
                     ptx::named_bar_sync(1, 128);
                     if (r < U.n)
                         a.ssq[(size_t)(U.p0 + r) * (a.d / AROWS) + U.mb] =
-                            ((part[r] + part[N + r]) + part[2 * N + r]) + part[3 * N + r];
+                            ((part[r] + part[NT + r]) + part[2 * NT + r]) + part[3 * NT + r];
                 }
             }
         }
@@ -724,26 +701,26 @@ int num_sms() {
     return n[dev];
 }
 
-template <int N, bool STMA>
-cudaError_t launch_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    using C = Cfg<N, STMA>;
-    CUtensorMap tm_w13, tm_w2, tm_xg, tm_h, tm_w13s, tm_w2s;
+template <bool STMA>
+cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    using C = Cfg<STMA>;
+    CUtensorMap tm_w13, tm_w2, tm_xq, tm_hq, tm_w13s, tm_w2s;
     const uint64_t P = (uint64_t)L.max_picks, E = s.E, d = s.d, I = s.I;
-    const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, BF = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16;
-    // w13 [E][2][I][d/2] as {64 bytes, I rows, 2E halves, d/128 slabs}
-    const uint64_t w13_d[4] = {64, I, 2 * E, d / 128}, w13_s[3] = {d / 2, I * d / 2, 64};
-    const uint32_t w13_b[4] = {64, 64, 2, 2};
-    // w2 [E d][I/2] as {64 bytes, E d rows, I/128 slabs}
-    const uint64_t w2_d[3] = {64, E * d, I / 128}, w2_s[2] = {I / 2, 64};
-    const uint32_t w2_b[3] = {64, AROWS, 2};
-    // xg [P][d] / h [P][I] bf16 as {64 elements, P rows, K/64 slabs}
-    const uint64_t xg_d[3] = {64, P, d / 64}, xg_s[2] = {d * 2, 128};
-    const uint64_t h_d[3] = {64, P, I / 64}, h_s[2] = {I * 2, 128};
-    const uint32_t tok_b[3] = {64, (uint32_t)N, 4};
-    if (!make_map(&tm_w13, U8, p.w13, 4, w13_d, w13_s, w13_b, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&tm_w2, U8, p.w2, 3, w2_d, w2_s, w2_b, CU_TENSOR_MAP_SWIZZLE_64B) ||
-        !make_map(&tm_xg, BF, p.ws + L.xg, 3, xg_d, xg_s, tok_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tm_h, BF, p.ws + L.h, 3, h_d, h_s, tok_b, CU_TENSOR_MAP_SWIZZLE_128B))
+    const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, U4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
+    // w13 [E][2][I][d/2] as 4-bit codes {128 codes, I rows, 2E halves, d/128 slabs}
+    const uint64_t w13_d[4] = {128, I, 2 * E, d / 128}, w13_s[3] = {d / 2, I * d / 2, 64};
+    const uint32_t w13_b[4] = {128, 64, 2, 2};
+    // w2 [E][d][I/2] as {128 codes, E d rows, I/128 slabs}
+    const uint64_t w2_d[3] = {128, E * d, I / 128}, w2_s[2] = {I / 2, 64};
+    const uint32_t w2_b[3] = {128, AROWS, 2};
+    // xq [2P][d] / hq [2P][I] e4m3 as {128 bytes, 2P rows, K/128 slabs}
+    const uint64_t xq_d[3] = {128, 2 * P, d / 128}, xq_s[2] = {d, 128};
+    const uint64_t hq_d[3] = {128, 2 * P, I / 128}, hq_s[2] = {I, 128};
+    const uint32_t tok_b[3] = {128, (uint32_t)NB, 2};
+    if (!make_map(&tm_w13, U4, p.w13, 4, w13_d, w13_s, w13_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_w2, U4, p.w2, 3, w2_d, w2_s, w2_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_xq, U8, p.ws + L.xq, 3, xq_d, xq_s, tok_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_hq, U8, p.ws + L.hq, 3, hq_d, hq_s, tok_b, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
     if (STMA) {
         // w13s [E][2][I][d/32] as {d/32 bytes, I rows, 2E halves}; w2s [E d][I/32]
@@ -758,20 +735,23 @@ cudaError_t launch_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
         tm_w13s = tm_w13;   // unused
         tm_w2s = tm_w2;
     }
-    cudaError_t e = cudaFuncSetAttribute(k_experts_tc<N, STMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_experts_mx<STMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     Args a;
     a.tiles = reinterpret_cast<const Tile*>(p.ws + L.tiles);
     a.sb = reinterpret_cast<StatusBlock*>(p.ws + L.status);
     a.w13s = p.w13s;
     a.w2s = p.w2s;
-    a.h = reinterpret_cast<__nv_bfloat16*>(p.ws + L.h);
+    a.hq = reinterpret_cast<uint8_t*>(p.ws + L.hq);
+    a.hs = reinterpret_cast<uint8_t*>(p.ws + L.hs);
     a.y = reinterpret_cast<float*>(p.ws + L.y);
     a.ssq = p.norm_w != nullptr ? reinterpret_cast<float*>(p.ws + L.ssq) : nullptr;
     a.tile_ready = reinterpret_cast<uint32_t*>(p.ws + L.tile_ready);
+    a.xs = reinterpret_cast<const uint8_t*>(p.ws + L.xs);
     a.d = s.d;
     a.I = s.I;
-    k_experts_tc<N, STMA><<<num_sms(), NUM_THREADS, C::SMEM, st>>>(tm_w13, tm_w2, tm_xg, tm_h, tm_w13s, tm_w2s, a);
+    a.P = L.max_picks;
+    k_experts_mx<STMA><<<num_sms(), NUM_THREADS, C::SMEM, st>>>(tm_w13, tm_w2, tm_xq, tm_hq, tm_w13s, tm_w2s, a);
     return cudaGetLastError();
 }
 
@@ -780,7 +760,7 @@ cudaError_t launch_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     timing_begin(K_EXPERTS, st);
     const bool stma = (s.d % 512 == 0) && (s.I % 512 == 0);
-    cudaError_t e = stma ? launch_tc<NT, true>(s, L, p, st) : launch_tc<NT, false>(s, L, p, st);
+    cudaError_t e = stma ? launch_mx<true>(s, L, p, st) : launch_mx<false>(s, L, p, st);
     timing_end(st);
     return e;
 }

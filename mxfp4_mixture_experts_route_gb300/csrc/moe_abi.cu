@@ -29,8 +29,12 @@ WsLayout ws_layout(const moe_shape& s) {
     L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
     L.active = take((size_t)s.E * 4);
     L.tile_ready = take((size_t)L.max_tiles * 4);
-    L.xg = take(P * s.d * 2);
-    L.h = take(P * s.I * 2);
+    // e4m3 hi / lo rows of the gathered tokens and of h, and their block scales
+    const size_t rows = P + NT;
+    L.xq = take(2 * P * s.d);
+    L.xs = take((size_t)((s.d + 255) / 256) * rows * TOKEN_SCALE_ROW);
+    L.hq = take(2 * P * s.I);
+    L.hs = take((size_t)((s.I + 255) / 256) * rows * TOKEN_SCALE_ROW);
     L.y = take(P * s.d * 4);
     L.ssq = take(P * (s.d / 128) * 4);                   // per-pick sums of y^2 by 128-row block
     L.xin = take((size_t)s.S * s.d * 2);                 // host-I/O staging
@@ -54,6 +58,7 @@ static int check_shape(const moe_shape* s) {
 }
 
 static bool a16(const void* p) { return ((uintptr_t)p & 15) == 0; }
+static bool a32(const void* p) { return ((uintptr_t)p & 31) == 0; }   // the 4-bit tensor maps' base rule
 
 static int check_ws(const moe_shape* s, void* ws, size_t ws_bytes) {
     if (!ws) return MOE_ERR_INVALID_ARG;
@@ -94,7 +99,7 @@ static int check_expert_args(const moe_shape* s, const void* x, const int32_t* i
                              const uint8_t* w2s, const float* norm_w, const float* out) {
     if (!x || !ids || !w || !w13 || !w13s || !w2 || !w2s || !out) return MOE_ERR_INVALID_ARG;
     if ((s->flags & MOE_POST_NORM) && !norm_w) return MOE_ERR_INVALID_ARG;
-    if (!a16(x) || !a16(ids) || !a16(w) || !a16(w13) || !a16(w13s) || !a16(w2) || !a16(w2s) || !a16(out))
+    if (!a16(x) || !a16(ids) || !a16(w) || !a32(w13) || !a16(w13s) || !a32(w2) || !a16(w2s) || !a16(out))
         return MOE_ERR_ALIGNMENT;
     if ((s->flags & MOE_POST_NORM) && !a16(norm_w)) return MOE_ERR_ALIGNMENT;
     return MOE_OK;
@@ -231,7 +236,7 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     if (!w_gate || !bias || !w13 || !w13s || !w2 || !w2s) return MOE_ERR_INVALID_ARG;
     if ((shape->flags & MOE_LOGIT_OFFSET) && !logit_off) return MOE_ERR_INVALID_ARG;
     if ((shape->flags & MOE_POST_NORM) && !norm_w) return MOE_ERR_INVALID_ARG;
-    if (!a16(w_gate) || !a16(bias) || !a16(w13) || !a16(w13s) || !a16(w2) || !a16(w2s))
+    if (!a16(w_gate) || !a16(bias) || !a32(w13) || !a16(w13s) || !a32(w2) || !a16(w2s))
         return MOE_ERR_ALIGNMENT;
     rc = check_ws(shape, ws, ws_bytes);
     if (!rc) rc = check_device();

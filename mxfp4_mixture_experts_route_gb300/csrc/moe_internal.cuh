@@ -29,6 +29,13 @@ static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
 // expert (the MMA N dimension; the pages' 16-row tiles, k5 page).
 constexpr int NT = 16;
 
+// Block scales of the gathered tokens and of h (e8m0, one per 32 elements):
+// a table [ceil(K/256) stages][P + NT picks][TOKEN_SCALE_ROW bytes], bytes
+// 0..7 of a row holding the stage's eight scales (16-byte rows, so that the
+// 16 rows of a tile are one aligned bulk copy; NT rows of padding so that the
+// last tile's copy stays inside the table).
+constexpr int TOKEN_SCALE_ROW = 16;
+
 // One work tile: expert e, first sorted pick p0, n picks (n <= NT).
 struct Tile {
     int32_t e, p0, n, pad;
@@ -36,7 +43,7 @@ struct Tile {
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, logits, counts, offsets, pos, src, tiles, active, tile_ready, xg, h, y, ssq;
+    size_t status, logits, counts, offsets, pos, src, tiles, active, tile_ready, xq, xs, hq, hs, y, ssq;
     size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
     size_t total;
     int max_tiles;

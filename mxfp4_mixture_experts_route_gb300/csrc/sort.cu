@@ -8,6 +8,7 @@
 // NT picks of one expert (k5 page: "Every row tile is 16 tokens").  Experts
 // without picks get no tile, so no weight byte of an untouched expert is read.
 #include "moe_internal.cuh"
+#include "tc_ptx.cuh"
 
 namespace moe {
 
@@ -202,28 +203,74 @@ __global__ void __launch_bounds__(SORT_WARPS * 32) k_sort(const int32_t* __restr
     }
 }
 
-// xg[p, :] = x[src[p] / k, :] for the valid picks p < n_picks, with the K
-// order inside every group of 8 elements rearranged to the MMA order of the
-// expert kernel's weight decode: positions (0..7) hold elements
-// (0, 4, 1, 5, 2, 6, 3, 7).  grid (max_picks), 128 threads, 16-byte copies.
-__global__ void __launch_bounds__(128) k_gather(const __nv_bfloat16* __restrict__ x,
-                                                const int32_t* __restrict__ src, int k, int d,
-                                                __nv_bfloat16* __restrict__ xg,
-                                                const StatusBlock* __restrict__ sb) {
+// Token rows of the expert GEMMs.  For every valid pick p < n_picks, token
+// t = src[p] / k: rows 2p and 2p + 1 of xq hold hi = e4m3(x[t] / 2^s) and
+// lo = e4m3(x[t] / 2^s - hi) for every 32-element block, and the scale table
+// xs holds the block's e8m0 byte s + 127, chosen so that the block's largest
+// magnitude divided by 2^s lies in [128, 256) (clamped to bytes 1..247).  For
+// a bf16 x the two rows add up to x / 2^s exactly, but for elements more than
+// 2^9 below the block maximum (there the error is below 2^-17 of it).  The
+// unused bytes of the last stage's scale rows of xs and hs (K / 32 not a
+// multiple of 8) are set to 127 (scale 1), as their codes are zero.
+// grid (max_picks), 128 threads; a thread takes 8 elements, four threads a
+// block.
+__global__ void __launch_bounds__(128) k_quant_gather(const __nv_bfloat16* __restrict__ x,
+                                                      const int32_t* __restrict__ src, int k, int d, int I, int P,
+                                                      uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+                                                      uint8_t* __restrict__ hs,
+                                                      const StatusBlock* __restrict__ sb) {
     const int p = blockIdx.x;
     const int sp = src[p];                 // read beside n_picks: src has max_picks entries
     if (p >= sb->n_picks) return;
     const int t = sp / k;
+    const size_t rows = (size_t)P + NT;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    uint4* o = reinterpret_cast<uint4*>(xg + (size_t)p * d);
-    for (int c = threadIdx.x; c < d / 8; c += blockDim.x) {
-        const uint4 v = __ldg(in + c);
-        uint4 w;
-        w.x = __byte_perm(v.x, v.z, 0x5410);   // elements 0, 4
-        w.y = __byte_perm(v.x, v.z, 0x7632);   // elements 1, 5
-        w.z = __byte_perm(v.y, v.w, 0x5410);   // elements 2, 6
-        w.w = __byte_perm(v.y, v.w, 0x7632);   // elements 3, 7
-        o[c] = w;
+    uint8_t* hi_row = xq + (size_t)(2 * p) * d;
+    uint8_t* lo_row = hi_row + d;
+    for (int c0 = 0; c0 < d / 8; c0 += blockDim.x) {
+        const int c = c0 + threadIdx.x;
+        const bool act = c < d / 8;        // whole blocks of four threads (d / 8 is a multiple of 16)
+        const uint4 v = act ? __ldg(in + c) : make_uint4(0, 0, 0, 0);
+        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
+        float f[8];
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            f[2 * j] = __uint_as_float(wv[j] << 16);
+            f[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
+        }
+        uint32_t amax = 0;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) amax = max(amax, __float_as_uint(fabsf(f[j])));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
+        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
+        int e = (int)((amax >> 23) & 0xFFu) - 7;
+        e = e < 1 ? 1 : (e > 247 ? 247 : e);
+        const float mult = __uint_as_float((uint32_t)(254 - e) << 23);   // 2^-(e - 127)
+        uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+            const float a0 = f[2 * j] * mult, a1 = f[2 * j + 1] * mult;
+            const uint32_t h2 = ptx::cvt_e4m3x2(a0, a1);
+            float b0, b1;
+            ptx::e4m3x2_to_f32(h2, b0, b1);
+            const uint32_t l2 = ptx::cvt_e4m3x2(a0 - b0, a1 - b1);
+            hw[j >> 1] |= h2 << (16 * (j & 1));
+            lw[j >> 1] |= l2 << (16 * (j & 1));
+        }
+        if (act) {
+            *reinterpret_cast<uint2*>(hi_row + 8 * c) = make_uint2(hw[0], hw[1]);
+            *reinterpret_cast<uint2*>(lo_row + 8 * c) = make_uint2(lw[0], lw[1]);
+            if ((c & 3) == 0) {
+                const int blk = c >> 2;
+                xs[((size_t)(blk >> 3) * rows + p) * TOKEN_SCALE_ROW + (blk & 7)] = (uint8_t)e;
+            }
+        }
+    }
+    if (threadIdx.x < 8) {
+        const int j = threadIdx.x;
+        const int nbx = d / 32, nbh = I / 32;
+        if ((nbx & 7) && j >= (nbx & 7)) xs[((size_t)(nbx >> 3) * rows + p) * TOKEN_SCALE_ROW + j] = 127;
+        if ((nbh & 7) && j >= (nbh & 7)) hs[((size_t)(nbh >> 3) * rows + p) * TOKEN_SCALE_ROW + j] = 127;
     }
 }
 
@@ -251,8 +298,10 @@ cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
     timing_begin(K_GATHER, st);
-    k_gather<<<L.max_picks, 128, 0, st>>>(p.x, reinterpret_cast<const int32_t*>(ws + L.src), s.k, s.d,
-                                          reinterpret_cast<__nv_bfloat16*>(ws + L.xg), sb);
+    k_quant_gather<<<L.max_picks, 128, 0, st>>>(p.x, reinterpret_cast<const int32_t*>(ws + L.src), s.k, s.d, s.I,
+                                                L.max_picks, reinterpret_cast<uint8_t*>(ws + L.xq),
+                                                reinterpret_cast<uint8_t*>(ws + L.xs),
+                                                reinterpret_cast<uint8_t*>(ws + L.hs), sb);
     timing_end(st);
     return cudaGetLastError();
 }

@@ -1,10 +1,11 @@
 // Inline-PTX wrappers for sm_100-family features used by the expert kernel:
-// mbarriers (with bounded waits), TMA tiled loads, cp.async with mbarrier
-// completion, and the 5th-generation tensor core (tcgen05: TMEM allocation,
-// register <-> TMEM copies, MMA with the A operand in TMEM, commit).
+// mbarriers (with bounded waits), TMA tiled and bulk loads, cp.async with
+// mbarrier completion, e4m3 conversions, and the 5th-generation tensor core
+// (tcgen05: TMEM allocation, register <-> TMEM copies, MMAs, commit).
 #pragma once
 
 #include <cuda.h>
+#include <cuda_fp16.h>
 #include <stdint.h>
 
 namespace moe {
@@ -296,6 +297,61 @@ __device__ __forceinline__ uint64_t smem_desc_sw128(uint32_t saddr) {
     d |= (uint64_t)1u << 46;                           // descriptor version
     d |= (uint64_t)2u << 61;                           // 128-byte swizzle
     return d;
+}
+
+// Block-scaled MMA, kind::mxf8f6f4 with one e8m0 scale per 32 K (scale_vec
+// 1X): D[tmem] (+)= (A * sfa) x (B * sfb), A and B from shared memory
+// (K-major descriptors), the scale vectors from TMEM.  Layout of the scales
+// in TMEM, for M = 128: row m of A reads lane m, column sfa + m / 32; column n
+// of B reads lane 32q + n of every lane quarter q, column sfb; the byte of
+// the 32-bit cell is the instruction descriptor's scale-factor id.
+__device__ __forceinline__ void mma_mx_ss(uint32_t d_tmem, uint64_t a_desc, uint64_t b_desc, uint32_t idesc,
+                                          uint32_t accumulate, uint32_t sfa_tmem, uint32_t sfb_tmem) {
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "setp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::mxf8f6f4.block_scale.scale_vec::1X [%0], %1, %2, %3, [%5], [%6], p;\n\t}"
+        ::"r"(d_tmem), "l"(a_desc), "l"(b_desc), "r"(idesc), "r"(accumulate), "r"(sfa_tmem), "r"(sfb_tmem)
+        : "memory");
+}
+
+// Instruction descriptor, kind::mxf8f6f4 block-scaled: A e2m1, B e4m3, e8m0
+// scales, fp32 accumulator, both K-major, M = m, N = n; asf / bsf pick the
+// byte of the scale cells (the K step within a group of four).
+__host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int m, int n, int asf, int bsf) {
+    return ((uint32_t)bsf << 4) | (5u << 7) | (0u << 10) | ((uint32_t)(n >> 3) << 17) | (1u << 23) |
+           ((uint32_t)(m >> 4) << 24) | ((uint32_t)asf << 29);
+}
+
+// 32 lanes x 4 consecutive 32-bit TMEM columns, all four set to v (taddr's
+// column a multiple of 4)
+__device__ __forceinline__ void tmem_st4_rep(uint32_t taddr, uint32_t v) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %1, %1, %1};" ::"r"(taddr), "r"(v) : "memory");
+}
+
+// Untiled bulk copy global -> shared, completing on an mbarrier (both
+// addresses 16-byte aligned, bytes a multiple of 16).
+__device__ __forceinline__ void bulk_load(void* dst, const void* src, uint32_t bytes, uint64_t* bar, uint64_t policy) {
+    asm volatile(
+        "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes.L2::cache_hint [%0], [%1], %2, [%3], %4;"
+        ::"r"(smem_u32(dst)), "l"(src), "r"(bytes), "r"(smem_u32(bar)), "l"(policy)
+        : "memory");
+}
+
+// Two fp32 -> two e4m3 (round to nearest even, saturating): lo -> bits 7..0,
+// hi -> bits 15..8.
+__device__ __forceinline__ uint32_t cvt_e4m3x2(float lo, float hi) {
+    uint16_t r;
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+    return r;
+}
+
+// Two e4m3 (bits 7..0 and 15..8) -> two fp32 (exact).
+__device__ __forceinline__ void e4m3x2_to_f32(uint32_t v, float& lo, float& hi) {
+    uint32_t h2;
+    asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(h2) : "h"((uint16_t)v));
+    lo = __half2float(__ushort_as_half((unsigned short)(h2 & 0xFFFFu)));
+    hi = __half2float(__ushort_as_half((unsigned short)(h2 >> 16)));
 }
 
 // Instruction descriptor, kind::f16: fp32 accumulator, bf16 A and B, both
