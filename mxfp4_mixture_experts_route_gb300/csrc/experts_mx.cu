@@ -25,13 +25,10 @@
 // epilogue adds each pick's two columns.
 //
 // One persistent CTA per SM, 12 warps:
-//   warp 0      weight producer: per 256-K stage of a unit, the weight tile
-//               (128 rows x 256 K e2m1 = 16 KB of HBM, 32 KB unpacked in
-//               shared memory; gate and up rows in one 4-D box) and its e8m0
-//               bytes into a ring of weight stages, and an L2 prefetch of the
-//               weight tile PF stages ahead (under full load the HBM latency
-//               is several microseconds, more than the shared memory covers at
-//               the bandwidth wanted).
+//   warp 0      weight producer: claims the CTA's next unit, and per 256-K
+//               stage of a unit loads the weight tile (128 rows x 256 K e2m1 =
+//               16 KB of HBM, 32 KB unpacked in shared memory; gate and up rows
+//               in one 4-D box) and its e8m0 bytes into a ring of weight stages.
 //   warp 7      token producer: the token tile (32 e4m3 rows x 256 K, one 3-D
 //               box of two 128-byte-swizzled slabs) and the tile's 16 rows of
 //               block scales (one bulk copy) into a ring of its own; for a
@@ -39,16 +36,22 @@
 //   warps 8-11  scale movers: copy the stage's weight and token block scales
 //               from shared memory into TMEM, in the layout the MMA reads.
 //   warps 1-2   MMA issuers (lane 0 of each): M = 128 weight rows, N = 32,
-//               K = 32; issuer m takes the 128-K half m of every stage into an
-//               fp32 accumulator of its own (double buffered by unit).
+//               K = 32; issuer m takes the stages of parity m of every unit
+//               into an fp32 accumulator of its own (double buffered by unit).
+//               One thread needs several hundred cycles per stage for its
+//               waits, MMAs and commits, more than a stage lasts at full HBM
+//               bandwidth; two issuers on alternate stages keep up.
 //   warps 3-6   epilogue: the issuers' accumulators and each pick's hi and lo
 //               column added; h = silu(g) * u split into e4m3 hi/lo rows with a
 //               block scale per 32 rows for gate_up; y (fp32) and per-128-row
 //               sums of squares for down.
-// Work units, in a static round-robin over the CTAs: gate_up units first
-// (64 gate rows stacked on the matching 64 up rows = one M = 128 operand), then
-// down units (128 rows of w2).  A down unit needs the h rows of its tile: the
-// counter of the tile, which every finished gate_up unit of it increments.
+// Work units, claimed by the CTAs from a device-wide counter (reset by the
+// sort kernel) so that a CTA that finishes early takes more: gate_up units
+// first (64 gate rows stacked on the matching 64 up rows = one M = 128
+// operand), then down units (128 rows of w2).  A down unit needs the h rows of
+// its tile: the counter of the tile, which every finished gate_up unit of it
+// increments.  Every gate_up unit is claimed before any down unit and a
+// gate_up unit waits on nothing, so each of these waits ends.
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
 
@@ -70,11 +73,7 @@ constexpr int BS_BYTES = NT * TOKEN_SCALE_ROW;   // the tile's token scale rows
 #ifndef MOE_MX_TOKEN_STAGES
 #define MOE_MX_TOKEN_STAGES 4
 #endif
-#ifndef MOE_MX_PREFETCH
-#define MOE_MX_PREFETCH 16
-#endif
 constexpr int NSB = MOE_MX_TOKEN_STAGES;     // token-tile stages
-constexpr int PF = MOE_MX_PREFETCH;          // L2 prefetch distance in weight stages
 constexpr int TMEM_COLS = 512;
 constexpr int NMMA = 2;                      // MMA-issuing warps (one thread each)
 constexpr int SF_COL0 = 2 * NMMA * NB;       // TMEM columns of the scale slots (after the accumulators)
@@ -128,7 +127,7 @@ struct Args {
 };
 
 struct Unit {
-    int down;        // 0: gate_up, 1: down
+    int down;        // 0: gate_up, 1: down, -1: no more units
     int tile, mb;    // tile index and row block
     int e, p0, n;
     int stages;      // 256-K stages of the unit
@@ -190,16 +189,26 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     StatusBlock* sb = a.sb;
+    // the weight producer's first two unit claims and the tile count, in
+    // flight during the set-up below
+    int claim0 = 0, claim1 = 0, n_tiles = 0;
+    if (warp == 0) {
+        n_tiles = sb->n_tiles;
+        if (lane == 0) {
+            claim0 = atomicAdd(&sb->work_next, 1);
+            claim1 = atomicAdd(&sb->work_next, 1);
+        }
+    }
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSA; ++i) {
             ptx::mbar_init(&full_a[i], STMA ? 1 : 1 + 32);   // expect_tx (+ 32 cp.async arrivals)
-            ptx::mbar_init(&empty_a[i], NMMA);
+            ptx::mbar_init(&empty_a[i], 1);                 // the stage's issuer
             ptx::mbar_init(&sf_full[i], 4);                 // the four scale movers
         }
         for (int i = 0; i < NSB; ++i) {
             ptx::mbar_init(&full_b[i], 1);
-            ptx::mbar_init(&empty_b[i], NMMA);
+            ptx::mbar_init(&empty_b[i], 1);
         }
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&acc_full[i], NMMA);
@@ -231,10 +240,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
 
-    const int n_tiles = sb->n_tiles;
-    const int U1 = n_tiles * (a.I / 64);
-    const int total = U1 + n_tiles * (a.d / AROWS);
-    const int my_units = total > (int)blockIdx.x ? (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1 : 0;
     const int mb1 = a.I / 64;
 
     auto fail = [&](int site) {
@@ -249,76 +254,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         if (lane == 0) ptx::mbar_arrive(&u_empty[i % UR]);
         return true;
     };
-    // unit i of this CTA without its tile entry (e, p0, n)
-    auto unit_shape = [&](int i, Unit& U) {
-        unit_coords(blockIdx.x + i * gridDim.x, U1, a, U.down, U.tile, U.mb);
-        U.stages = ((U.down ? a.I : a.d) + KS - 1) / KS;
-    };
 
     if (warp == 0) {
         // ------------------------------------------------------------ weight producer
         const uint64_t pol_w = ptx::policy_evict_first();
-        // L2 prefetch cursor: unit pi, stage pc, PF stages ahead of the loads
-        int pi = 0, pc = 0;
-        Unit PU;
-        Tile pnext = {0, 0, 0, 0};
-        if (my_units > 0) {
-            unit_shape(0, PU);
-            PU.e = a.tiles[PU.tile].e;
-            if (my_units > 1) {
-                Unit t;
-                unit_shape(1, t);
-                pnext = a.tiles[t.tile];
-            }
-        }
-        auto prefetch_one = [&]() {
-            if (pi >= my_units) return;
-            if (lane == 0) {
-                if (!PU.down) {
-                    const int r0 = PU.mb * 64;
-                    ptx::tma_prefetch_4d(&tm_w13, 0, r0, 2 * PU.e, 2 * pc);
-                    if (STMA && !(pc & 1)) ptx::tma_prefetch_3d(&tm_w13s, (pc >> 1) * 16, r0, 2 * PU.e);
-                } else {
-                    const int r0 = PU.e * a.d + PU.mb * AROWS;
-                    ptx::tma_prefetch_3d(&tm_w2, 0, r0, 2 * pc);
-                    if (STMA && !(pc & 1)) ptx::tma_prefetch_2d(&tm_w2s, (pc >> 1) * 16, r0);
-                }
-            }
-            if (++pc == PU.stages) {
-                pc = 0;
-                if (++pi < my_units) {
-                    unit_shape(pi, PU);
-                    PU.e = pnext.e;
-                    if (pi + 1 < my_units) {
-                        Unit t;
-                        unit_shape(pi + 1, t);
-                        pnext = a.tiles[t.tile];
-                    }
-                }
-            }
-        };
-        for (int j = 0; j < PF; ++j) prefetch_one();
-
+        const int U1 = n_tiles * mb1;
+        const int total = U1 + n_tiles * (a.d / AROWS);
+        auto tile_of = [&](int u) { return u < U1 ? u / mb1 : (u - U1) / (a.d / AROWS); };
+        // unit u and its tile entry; the claim of the next unit (issued one unit
+        // earlier) and then the one after it stay in flight while a unit is issued
+        int u = __shfl_sync(0xffffffffu, claim0, 0);
+        int next_claim = claim1;   // lane 0
+        Tile tl = {0, 0, 0, 0}, tl_next = {0, 0, 0, 0};
+        if (u < total) tl = a.tiles[tile_of(u)];
         int ts = 0;   // stage sequence number
         bool ok = true;
-        Tile tnext = {0, 0, 0, 0};
-        if (my_units > 0) {
-            Unit t;
-            unit_shape(0, t);
-            tnext = a.tiles[t.tile];
-        }
-        for (int i = 0; i < my_units && ok; ++i) {
+        for (int i = 0; ok; ++i) {
             Unit U;
-            unit_shape(i, U);
-            U.e = tnext.e;
-            U.p0 = tnext.p0;
-            U.n = tnext.n;
-            U.pad = 0;
-            if (i + 1 < my_units) {   // the next unit's tile entry, in flight while this one is issued
-                Unit t;
-                unit_shape(i + 1, t);
-                tnext = a.tiles[t.tile];
+            if (u < total) {
+                unit_coords(u, U1, a, U.down, U.tile, U.mb);
+                U.e = tl.e;
+                U.p0 = tl.p0;
+                U.n = tl.n;
+                U.stages = ((U.down ? a.I : a.d) + KS - 1) / KS;
+            } else {
+                U.down = -1;
+                U.tile = U.mb = U.e = U.p0 = U.n = U.stages = 0;
             }
+            U.pad = 0;
+            const int u_next = u < total ? __shfl_sync(0xffffffffu, next_claim, 0) : total;
+            if (u_next < total) tl_next = a.tiles[tile_of(u_next)];
+            if (lane == 0) next_claim = u_next < total ? atomicAdd(&sb->work_next, 1) : total;
             if (!ptx::mbar_wait_warp(&u_empty[i % UR], ((i / UR) & 1) ^ 1, abort_flag, WAIT_NS)) {
                 if (lane == 0) fail(8);
                 break;
@@ -327,6 +293,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uring[i % UR] = U;
                 ptx::mbar_arrive(&u_full[i % UR]);
             }
+            if (U.down < 0) break;
             const int K = U.down ? a.I : a.d;
             const int r0 = U.down ? U.e * a.d + U.mb * AROWS : U.mb * 64;
             for (int c = 0; c < U.stages; ++c, ++ts) {
@@ -366,9 +333,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     }
                     ptx::cp_async_mbar_arrive_noinc(&full_a[s]);
                 }
-                prefetch_one();
                 __syncwarp();
             }
+            u = u_next;
+            tl = tl_next;
         }
         ptx::cp_async_wait_all();
     } else if (warp == TOK_WARP) {
@@ -377,12 +345,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const size_t tab_rows = (size_t)a.P + NT;
         int ts = 0;
         bool ok = true;
-        for (int i = 0; i < my_units && ok; ++i) {
+        for (int i = 0; ok; ++i) {
             Unit U;
             if (!take_unit(i, U)) {
                 if (lane == 0) fail(12);
                 break;
             }
+            if (U.down < 0) break;
             const CUtensorMap* tmB = U.down ? &tm_hq : &tm_xq;
             const uint8_t* tab = U.down ? a.hs : a.xs;
             if (U.down) {
@@ -428,12 +397,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_base = (uint32_t)(32 * q) << 16;
         int ts = 0;
         bool ok = true;
-        for (int i = 0; i < my_units && ok; ++i) {
+        for (int i = 0; ok; ++i) {
             Unit U;
             if (!take_unit(i, U)) {
                 if (lane == 0) fail(10);
                 break;
             }
+            if (U.down < 0) break;
             for (int c = 0; c < U.stages; ++c, ++ts) {
                 const int s = ts % NSA, sbi = ts % NSB;
                 if (!ptx::mbar_wait_warp(&full_a[s], (ts / NSA) & 1, abort_flag, WAIT_NS) ||
@@ -466,45 +436,54 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp >= MMA_WARP0 && warp < MMA_WARP0 + NMMA) {
         // ------------------------------------------------------------ MMA issuers
-        const int m = warp - MMA_WARP0;   // this issuer takes the 128-K half m of every stage
+        // Issuer m takes the stages c of every unit with c mod 2 == m (all
+        // eight K steps of each), so the two issue loops overlap on different
+        // stages.  It waits only on sf_full: the scale movers arrive there
+        // after they have waited on the stage's weight and token barriers, so
+        // both TMA copies are complete and visible once sf_full completes.
+        const int m = warp - MMA_WARP0;
         int ts = 0;
-        for (int i = 0; i < my_units; ++i) {
+        for (int i = 0;; ++i) {
             Unit U;
             if (!take_unit(i, U)) {
                 if (lane == 0) fail(9);
                 break;
             }
+            if (U.down < 0) break;
             bool ok = true;
             if (lane == 0) {
                 const int ab = i & 1;
                 const uint32_t d_tmem = tmem + (ab * NMMA + m) * NB;
-                for (int c = 0; c < U.stages && ok; ++c, ++ts) {
+                for (int c = 0; c < U.stages; ++c, ++ts) {
+                    if ((c & 1) != m) continue;
                     const int s = ts % NSA, sbi = ts % NSB;
-                    if (c == 0 && !ptx::mbar_wait(&acc_empty[ab], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
+                    if (c == m && !ptx::mbar_wait(&acc_empty[ab], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
                         fail(3);
                         ok = false;
                         break;
                     }
-                    if (!ptx::mbar_wait(&full_a[s], (ts / NSA) & 1, abort_flag, WAIT_NS) ||
-                        !ptx::mbar_wait(&full_b[sbi], (ts / NSB) & 1, abort_flag, WAIT_NS) ||
-                        !ptx::mbar_wait(&sf_full[s], (ts / NSA) & 1, abort_flag, WAIT_NS)) {
+                    if (!ptx::mbar_wait(&sf_full[s], (ts / NSA) & 1, abort_flag, WAIT_NS)) {
                         fail(4);
                         ok = false;
                         break;
                     }
                     ptx::tc_fence_after();
-                    const uint32_t a0 = ptx::smem_u32(wst + s * C::A_STAGE) + m * A_SLAB;
-                    const uint32_t b0 = ptx::smem_u32(tst + sbi * C::B_STAGE) + m * B_SLAB;
+                    const uint32_t a0 = ptx::smem_u32(wst + s * C::A_STAGE);
+                    const uint32_t b0 = ptx::smem_u32(tst + sbi * C::B_STAGE);
                     const uint32_t col = SF_COL0 + s * SF_SLOT;
 #pragma unroll
-                    for (int j = 0; j < 4; ++j) {
-                        ptx::mma_mx_ss(d_tmem, ptx::smem_desc_sw128(a0 + 32 * j), ptx::smem_desc_sw128(b0 + 32 * j),
-                                       ptx::idesc_mx_e2m1_e4m3(AROWS, NB, j, j), (c > 0 || j > 0) ? 1u : 0u,
-                                       tmem + col + SF_A1 * m, tmem + col + SF_B0 + (SF_B1 - SF_B0) * m);
+                    for (int kk = 0; kk < KS / 32; ++kk) {
+                        const int h = kk >> 2, j = kk & 3;   // 128-K slab, K step within it
+                        ptx::mma_mx_ss(d_tmem, ptx::smem_desc_sw128(a0 + h * A_SLAB + 32 * j),
+                                       ptx::smem_desc_sw128(b0 + h * B_SLAB + 32 * j),
+                                       ptx::idesc_mx_e2m1_e4m3(AROWS, NB, j, j), (c > m || kk > 0) ? 1u : 0u,
+                                       tmem + col + SF_A1 * h, tmem + col + SF_B0 + (SF_B1 - SF_B0) * h);
                     }
                     ptx::mma_commit(&empty_a[s]);
                     ptx::mma_commit(&empty_b[sbi]);
                 }
+                // an issuer without a stage in this unit (one-stage units) commits
+                // nothing of its own; the epilogue reads only the issuers that had one
                 if (ok) ptx::mma_commit(&acc_full[ab]);
             }
             ts = __shfl_sync(0xffffffffu, ts, 0);
@@ -522,26 +501,31 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int r = 32 * qd + lane;
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
         const size_t tab_rows = (size_t)a.P + NT;
-        for (int i = 0; i < my_units; ++i) {
+        for (int i = 0;; ++i) {
             const int ab = i & 1;
             // the four epilogue warps take one decision before their named
-            // barriers: carry on, or leave together
+            // barriers: carry on, or leave together (they all read the same
+            // ring entry, so they all see the end of the units together)
             Unit U;
-            if (!take_unit(i, U) && lane == 0) fail(11);
-            if (!*abort_flag && !ptx::mbar_wait_warp(&acc_full[ab], (i >> 1) & 1, abort_flag, WAIT_NS) &&
+            const bool got = take_unit(i, U);
+            if (!got && lane == 0) fail(11);
+            const bool end = got && U.down < 0;
+            if (!end && !*abort_flag && !ptx::mbar_wait_warp(&acc_full[ab], (i >> 1) & 1, abort_flag, WAIT_NS) &&
                 lane == 0)
                 fail(7);
             ptx::named_bar_sync(1, 128);
             if (threadIdx.x == EPI_WARP0 * 32) *epi_flag = *abort_flag;
             ptx::named_bar_sync(1, 128);
-            if (*epi_flag) break;
+            if (*epi_flag || end) break;
             ptx::tc_fence_after();
-            // v[n]: both issuers' halves of K, hi + lo column of pick n
+            // v[n]: the issuers' stages, hi + lo column of pick n
             float v[NT];
 #pragma unroll
             for (int n = 0; n < NT; ++n) v[n] = 0.f;
+            const int n_iss = U.stages < NMMA ? U.stages : NMMA;   // issuers that had a stage
 #pragma unroll
             for (int mm = 0; mm < NMMA; ++mm) {
+                if (mm >= n_iss) break;
                 uint32_t t[NB];
 #pragma unroll
                 for (int j = 0; j < NB / 16; ++j)
