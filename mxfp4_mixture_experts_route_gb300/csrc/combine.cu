@@ -26,6 +26,8 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* __restrict_
                                                         const int32_t* __restrict__ pos, const float* __restrict__ w,
                                                         const float* __restrict__ norm_w, float eps, int k, int d,
                                                         float* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
     const int t = blockIdx.x;
     __shared__ float coef[CB_MAXK];
     __shared__ int32_t prow[CB_MAXK];
@@ -89,12 +91,12 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* __restrict_
 cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     timing_begin(K_COMBINE, st);
     const dim3 grid(s.S, (s.d + CB_COLS - 1) / CB_COLS);
-    k_combine<<<grid, CB_THREADS, 0, st>>>(reinterpret_cast<const float*>(p.ws + L.y),
-                                           reinterpret_cast<const float*>(p.ws + L.ssq),
-                                           reinterpret_cast<const int32_t*>(p.ws + L.pos), p.weights, p.norm_w,
-                                           s.norm_eps, s.k, s.d, p.out);
+    const cudaError_t e =
+        launch_pdl(k_combine, grid, dim3(CB_THREADS), 0, st, reinterpret_cast<const float*>(p.ws + L.y),
+                   reinterpret_cast<const float*>(p.ws + L.ssq), reinterpret_cast<const int32_t*>(p.ws + L.pos),
+                   (const float*)p.weights, p.norm_w, s.norm_eps, s.k, s.d, p.out);
     timing_end(st);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

@@ -189,16 +189,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     StatusBlock* sb = a.sb;
-    // the weight producer's first two unit claims and the tile count, in
-    // flight during the set-up below
-    int claim0 = 0, claim1 = 0, n_tiles = 0;
-    if (warp == 0) {
-        n_tiles = sb->n_tiles;
-        if (lane == 0) {
-            claim0 = atomicAdd(&sb->work_next, 1);
-            claim1 = atomicAdd(&sb->work_next, 1);
-        }
-    }
+    pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSA; ++i) {
@@ -234,6 +225,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == TOK_WARP && lane == 0) {
         ptx::prefetch_tensormap(&tm_xq);
         ptx::prefetch_tensormap(&tm_hq);
+    }
+    // the set-up above needs nothing from the preceding kernels; everything
+    // below reads their results
+    pdl_wait();
+    // the weight producer's first two unit claims and the tile count
+    int claim0 = 0, claim1 = 0, n_tiles = 0;
+    if (warp == 0) {
+        n_tiles = sb->n_tiles;
+        if (lane == 0) {
+            claim0 = atomicAdd(&sb->work_next, 1);
+            claim1 = atomicAdd(&sb->work_next, 1);
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -735,8 +738,8 @@ cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
     a.d = s.d;
     a.I = s.I;
     a.P = L.max_picks;
-    k_experts_mx<STMA><<<num_sms(), NUM_THREADS, C::SMEM, st>>>(tm_w13, tm_w2, tm_xq, tm_hq, tm_w13s, tm_w2s, a);
-    return cudaGetLastError();
+    return launch_pdl(k_experts_mx<STMA>, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, tm_w13, tm_w2, tm_xq, tm_hq,
+                      tm_w13s, tm_w2s, a);
 }
 
 }  // namespace

@@ -117,6 +117,20 @@ static int run_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cud
     return cuda_rc(launch_combine(s, L, p, st));
 }
 
+// The whole block.  At small S the top-k and the sort share one kernel (one
+// launch and one global round trip of the ids fewer).
+static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    if (!topk_sort_fits(s)) {
+        const int rc = run_route(s, L, p, st);
+        return rc ? rc : run_experts(s, L, p, st);
+    }
+    int rc = cuda_rc(launch_router_logits(s, L, p, st));
+    if (!rc) rc = cuda_rc(launch_topk_sort_gather(s, L, p, st));
+    if (!rc) rc = cuda_rc(launch_experts(s, L, p, st));
+    if (!rc) rc = cuda_rc(launch_combine(s, L, p, st));
+    return rc;
+}
+
 }  // namespace moe
 
 using namespace moe;
@@ -135,7 +149,7 @@ const char* moe_strerror(int code) {
         case MOE_ERR_CUDA: return "CUDA error";
         case MOE_ERR_TIMEOUT: return "device wait timed out";
         case MOE_ERR_BAD_IDS: return "expert id out of range or repeated within a token";
-        case MOE_ERR_BAD_SCALE: return "e8m0 scale byte above 128";
+        case MOE_ERR_BAD_SCALE: return "e8m0 scale byte 255 (NaN)";
         case MOE_ERR_NO_DEVICE: return "no sm_103 device";
         default: return "unknown status";
     }
@@ -220,10 +234,7 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate, const
     p.weights = weights;
     p.out = out;
     p.ws = (char*)ws;
-    cudaStream_t st = (cudaStream_t)stream;
-    rc = run_route(*shape, L, p, st);
-    if (rc) return rc;
-    return run_experts(*shape, L, p, st);
+    return run_forward(*shape, L, p, (cudaStream_t)stream);
 }
 
 int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_gate, const float* bias,

@@ -8,6 +8,8 @@
 
 #include "moe.h"
 
+#include <utility>
+
 namespace moe {
 
 // ---------------------------------------------------------------------------
@@ -59,10 +61,38 @@ __device__ __forceinline__ void latch_status(StatusBlock* sb, int code, int deta
 }
 
 // ---------------------------------------------------------------------------
+// Programmatic dependent launch.  The block's kernels are launched so that the
+// next one may start while its predecessor is still running: every kernel
+// allows its successor to launch at once (pdl_trigger), does the set-up that
+// needs no predecessor's data, and calls pdl_wait, which returns when the
+// predecessor grid has completed and its writes are visible, before it reads
+// or writes anything the stream's earlier kernels touch.  Without the launch
+// attribute (or after a non-kernel stream operation) pdl_wait returns at once.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+
+template <typename... KArgs, typename... Args>
+cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t smem, cudaStream_t st,
+                       Args&&... args) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    return cudaLaunchKernelEx(&cfg, kern, std::forward<Args>(args)...);
+}
+
+// ---------------------------------------------------------------------------
 // per-kernel timing hooks (moe_timing_*): no-ops unless enabled
 // ---------------------------------------------------------------------------
 enum KernelId {
-    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_NUM
+    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_TOPK_SORT, K_NUM
 };
 void timing_begin(int kernel_id, cudaStream_t st);
 void timing_end(cudaStream_t st);
@@ -86,7 +116,11 @@ struct Ptrs {
     char* ws;
 };
 
+cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+// moe_forward at small S: top-k and sort in one kernel (needs the logits)
+bool topk_sort_fits(const moe_shape& s);
+cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);

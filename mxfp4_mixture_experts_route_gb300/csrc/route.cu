@@ -15,6 +15,7 @@
 // fixed order.  One warp a token then does the selection (the k3 "every CTA
 // routes every token" redundancy is not needed: the ids are produced once).
 #include "moe_internal.cuh"
+#include "topk.cuh"
 
 #include <cooperative_groups.h>
 
@@ -53,6 +54,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
     const int k_begin = (int)((long long)nk * ks / kslices) * 128;
     const int k_end = (int)((long long)nk * (ks + 1) / kslices) * 128;
     const int nt = min(RT_TOKENS, S - t0);
+    pdl_trigger();
     float acc[RT_TOKENS];
 #pragma unroll
     for (int t = 0; t < RT_TOKENS; ++t) acc[t] = 0.f;
@@ -61,6 +63,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
         const int q16 = klen / 8;                            // 16-byte pieces of a row slice
         uint4 w = make_uint4(0, 0, 0, 0);
         if (e < E && lane < q16) w = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)e * d + kc) + lane);
+        if (kc == k_begin) pdl_wait();   // the first weight slice is in flight; x may come from the stream's last kernel
         __syncthreads();
         for (int i = threadIdx.x; i < nt * q16; i += RT_THREADS) {
             const int r = i / q16, c = i % q16;
@@ -108,71 +111,19 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
     cluster.sync();   // every CTA keeps its shared memory until the first has read it
 }
 
-// One warp per token: s = sigmoid(L), sel = s + bias, k rounds of a warp argmax (ties -> lower
-// expert id), then the picks in ascending id with w_j = s_j / sum s.  Lane l
-// holds experts l, l+32, ... (E <= 512).
+// One warp per token (see topk_token).
 __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ L, const float* __restrict__ bias,
                                               int S, int E, int k, int32_t* __restrict__ ids,
                                               float* __restrict__ wout) {
     const int lane = threadIdx.x & 31;
+    pdl_trigger();
+    pdl_wait();
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
     if (t >= S) return;
-    constexpr int MAXE = 512 / 32;
-    float s[MAXE], sel[MAXE], z[MAXE];
-#pragma unroll
-    for (int i = 0; i < MAXE; ++i) {           // independent loads, all in flight together
-        const int e = lane + 32 * i;
-        z[i] = e < E ? L[(size_t)t * E + e] : 0.f;
-    }
-#pragma unroll
-    for (int i = 0; i < MAXE; ++i) {
-        const int e = lane + 32 * i;
-        if (e < E) {
-            s[i] = 1.0f / (1.0f + expf(-z[i]));
-            const float v = s[i] + bias[e];
-            sel[i] = (v == v) ? v : -INFINITY;
-        } else {
-            s[i] = 0.f;
-            sel[i] = -INFINITY;
-        }
-    }
-    int my_id = 0x7fffffff;   // lane j < k keeps pick j
-    float my_s = 0.f;
-    for (int r = 0; r < k; ++r) {
-        float bv = -INFINITY;
-        int bi = 0x7fffffff;
-#pragma unroll
-        for (int i = 0; i < MAXE; ++i) {
-            const int e = lane + 32 * i;
-            if (e < E && (sel[i] > bv || (sel[i] == bv && e < bi))) { bv = sel[i]; bi = e; }
-        }
-#pragma unroll
-        for (int m = 16; m >= 1; m >>= 1) {
-            const float ov = __shfl_xor_sync(0xffffffffu, bv, m);
-            const int oi = __shfl_xor_sync(0xffffffffu, bi, m);
-            if (ov > bv || (ov == bv && oi < bi)) { bv = ov; bi = oi; }
-        }
-        // the owner lane retires the winner and broadcasts its unbiased score
-        const int owner = bi & 31, slot = bi >> 5;
-        float sv = 0.f;
-#pragma unroll
-        for (int i = 0; i < MAXE; ++i)
-            if (lane == owner && i == slot) { sv = s[i]; sel[i] = -INFINITY; }
-        sv = __shfl_sync(0xffffffffu, sv, owner);
-        if (lane == r) { my_id = bi; my_s = sv; }
-    }
-    // ascending id order: rank of my pick among the k picks
-    float tot = 0.f;
-    int rank = 0;
-    for (int j = 0; j < k; ++j) {
-        const int oid = __shfl_sync(0xffffffffu, my_id, j);
-        tot += __shfl_sync(0xffffffffu, my_s, j);
-        rank += (oid < my_id) ? 1 : 0;
-    }
-    if (lane < k) {
-        ids[(size_t)t * k + rank] = my_id;
-        wout[(size_t)t * k + rank] = my_s / tot;
-    }
+    if (E <= 256)
+        topk_token<256 / 32>(L + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
+    else
+        topk_token<512 / 32>(L + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
 }
 
 }  // namespace
@@ -187,7 +138,7 @@ int router_kslices(const moe_shape& s, int num_sms) {
     return ks;
 }
 
-cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     float* logits = reinterpret_cast<float*>(p.ws + L.logits);
     const int ks = L.router_kslices;
     cudaLaunchConfig_t cfg = {};
@@ -195,23 +146,30 @@ cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, c
     cfg.blockDim = dim3(RT_THREADS);
     cfg.dynamicSmemBytes = 0;
     cfg.stream = st;
-    cudaLaunchAttribute attr[1];
+    cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
     attr[0].val.clusterDim.x = 1;
     attr[0].val.clusterDim.y = ks;
     attr[0].val.clusterDim.z = 1;
+    attr[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = 2;
     timing_begin(K_ROUTER, st);
     cudaError_t e = cudaLaunchKernelEx(&cfg, k_router, p.x, p.w_gate, p.logit_off, logits, s.S, s.d, s.E, ks);
     timing_end(st);
+    return e;
+}
+
+cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    cudaError_t e = launch_router_logits(s, L, p, st);
     if (e != cudaSuccess) return e;
     const int warps_per_block = 8;
     timing_begin(K_TOPK, st);
-    k_topk<<<(s.S + warps_per_block - 1) / warps_per_block, 32 * warps_per_block, 0, st>>>(
-        logits, p.bias, s.S, s.E, s.k, p.ids, p.weights);
+    e = launch_pdl(k_topk, dim3((s.S + warps_per_block - 1) / warps_per_block), dim3(32 * warps_per_block), 0, st,
+                   reinterpret_cast<const float*>(p.ws + L.logits), p.bias, s.S, s.E, s.k, p.ids, p.weights);
     timing_end(st);
-    return cudaGetLastError();
+    return e;
 }
 
 }  // namespace moe

@@ -3,204 +3,197 @@
 // vllm.models.muse_spark.amd.mono.kernels.k3, dn_loads: "Task (u, j)'s w2
 // operands ... expert etab[u], u clamped below nv" -- the pages keep a table of
 // the local experts that have picks and run tasks (expert, tile).  Here that
-// table is built once per call: picks are counted per expert, sorted by
-// (expert, token) with a stable counting sort, and cut into tiles of at most
-// NT picks of one expert (k5 page: "Every row tile is 16 tokens").  Experts
-// without picks get no tile, so no weight byte of an untouched expert is read.
+// table is built once per call: picks are counted per expert, placed in one
+// segment per expert, and each segment is cut into tiles of at most NT picks
+// (k5 page: "Every row tile is 16 tokens").  Experts without picks get no
+// tile, so no weight byte of an untouched expert is read.
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
+#include "topk.cuh"
+
+#include <algorithm>
 
 namespace moe {
 
 namespace {
 
-constexpr int MAX_K = 16;
+constexpr int SORT_THREADS = 1024;
 
-// One CTA of SORT_WARPS warps.  Warp w owns a range of 32-token groups and
-// walks it with lane = token.
-//   pass 1: validate ids, per-warp per-expert counts (smem)
-//   pass 2: per-expert exclusive scan over warps, scan over experts -> offsets,
-//           tile schedule, active list
-//   pass 3: positions: offset[e] + base[w][e] + rank among earlier tokens of
-//           the group that picked e (a 32-bit lane mask per expert)
-// Output: counts[E], offsets[E+1], pos[t*k+j] (-1 for an invalid pick),
-// src[p] = t*k+j, tiles[], active[], and n_picks / n_tiles / n_active.
-// Global memory is only read for the ids (all of a token's ids in flight at
-// once); everything the passes share stays in shared memory.
-template <int SORT_WARPS>
-__global__ void __launch_bounds__(SORT_WARPS * 32) k_sort(const int32_t* __restrict__ ids, int S, int E, int k,
-                                                          int32_t* __restrict__ counts,
-                                                          int32_t* __restrict__ offsets,
-                                                          int32_t* __restrict__ pos, int32_t* __restrict__ src,
-                                                          Tile* __restrict__ tiles, int32_t* __restrict__ active,
-                                                          uint32_t* __restrict__ tile_ready, int max_tiles,
-                                                          StatusBlock* __restrict__ sb) {
-    constexpr int SORT_THREADS = SORT_WARPS * 32;
-    extern __shared__ int32_t smem[];
-    int32_t* cnt = smem;                        // [SORT_WARPS][E]
-    uint32_t* mask = reinterpret_cast<uint32_t*>(smem + SORT_WARPS * E);  // [SORT_WARPS][E]
-    int32_t* etot = smem + 2 * SORT_WARPS * E;  // [E] totals, then exclusive offsets
-    int32_t* etil = etot + E;                   // [E] tiles per expert, then tile offsets
-    int32_t* eact = etil + E;                   // [E] active flag, then active slot
-    int32_t* ecnt = eact + E;                   // [E] picks per expert
-    __shared__ int32_t scan_tmp[32];
+struct SortOut {
+    int32_t* counts;
+    int32_t* offsets;
+    int32_t* pos;
+    int32_t* src;
+    Tile* tiles;
+    int32_t* active;
+    uint32_t* tile_ready;
+    int max_tiles;
+    StatusBlock* sb;
+};
 
-    const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
-    for (int i = tid; i < 2 * SORT_WARPS * E; i += SORT_THREADS) smem[i] = 0;
-    for (int i = tid; i < max_tiles; i += SORT_THREADS) tile_ready[i] = 0u;
+// shared-memory ints of sort_picks: per expert a count, a segment offset and a
+// tile offset (E + 1 each)
+__host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
+
+// Sort of the S * k picks by expert, one CTA of SORT_THREADS threads.
+//   1. every pick p = t*k + j whose id e is in [0, E) and not repeated by an
+//      earlier pick of token t takes a rank within expert e (a shared-memory
+//      atomic); the others get pos[p] = -1 and latch MOE_ERR_BAD_IDS
+//   2. one warp scans the counts over the experts: segment offsets, tile
+//      offsets and active-expert slots
+//   3. every thread places its picks (pos[p] = offset[e] + rank, src[pos] = p)
+//      and writes tile entries (expert e, first pick, picks in the tile)
+// The order of the picks inside a segment is the order the atomics came in:
+// each pick is an independent column of the expert GEMMs, so the results do
+// not depend on it.  ids may be in global or shared memory.
+// Output: counts[E], offsets[E+1], pos[S*k], src[n_picks], tiles[n_tiles],
+// active[n_active] and n_picks / n_tiles / n_active; tile_ready[] zeroed.
+__device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int k, const SortOut& o,
+                                           int32_t* smem) {
+    int32_t* cnt = smem;               // [E + 1] counts
+    int32_t* off = cnt + (E + 1);      // [E + 1] segment offsets
+    int32_t* toff = off + (E + 1);     // [E + 1] tile offsets
+    __shared__ int32_t tot_tiles;
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = S * k;
+    StatusBlock* sb = o.sb;
+
+    for (int i = tid; i <= E; i += SORT_THREADS) cnt[i] = 0;
+    for (int i = tid; i < o.max_tiles; i += SORT_THREADS) o.tile_ready[i] = 0u;
     __syncthreads();
 
-    const int groups = (S + 31) / 32;
-    const int gpw = (groups + SORT_WARPS - 1) / SORT_WARPS;   // groups per warp
-    const int g0 = warp * gpw, g1 = min(groups, g0 + gpw);
-
-    // token t's k ids; bit j of the result is set when pick j is an id in
-    // [0, E) that no earlier pick of the token repeats
-    auto load_ids = [&](int t, int* my) -> uint32_t {
-#pragma unroll
-        for (int j = 0; j < MAX_K; ++j) my[j] = (j < k) ? __ldg(ids + (size_t)t * k + j) : -1;
-        uint32_t valid = 0;
-#pragma unroll
-        for (int j = 0; j < MAX_K; ++j) {
-            bool ok = j < k && my[j] >= 0 && my[j] < E;
-#pragma unroll
-            for (int q = 0; q < j; ++q) ok = ok && (my[q] != my[j]);
-            valid |= ok ? 1u << j : 0u;
+    // 1 ----------------------------------------------------------------------
+    // the lanes of a warp that hold the same expert share one atomic
+    const uint32_t lower = (1u << lane) - 1u;
+    for (int p0 = warp * 32; p0 < P; p0 += SORT_THREADS) {
+        const int p = p0 + lane;
+        int e = -1;
+        bool ok = false;
+        if (p < P) {
+            const int t = p / k, j = p - t * k;
+            e = ids[p];
+            ok = e >= 0 && e < E;
+            for (int q = 0; q < j && ok; ++q) ok = ids[(size_t)t * k + q] != e;
         }
-        return valid;
-    };
-
-    // pass 1 ------------------------------------------------------------
-    for (int g = g0; g < g1; ++g) {
-        const int t = g * 32 + lane;
-        if (t < S) {
-            int my[MAX_K];
-            const uint32_t valid = load_ids(t, my);
-#pragma unroll
-            for (int j = 0; j < MAX_K; ++j) {
-                if (valid >> j & 1u) atomicAdd(&cnt[warp * E + my[j]], 1);
-                else if (j < k) latch_status(sb, MOE_ERR_BAD_IDS, t * k + j);
+        const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+        const int leader = __ffs(grp) - 1;
+        int base = 0;
+        if (ok && lane == leader) base = atomicAdd(&cnt[e], __popc(grp));
+        base = __shfl_sync(0xffffffffu, base, leader);
+        if (p < P) {
+            if (ok) {
+                o.pos[p] = base + __popc(grp & lower);   // rank within the expert, for now
+            } else {
+                o.pos[p] = -1;
+                latch_status(sb, MOE_ERR_BAD_IDS, p);
             }
         }
     }
     __syncthreads();
 
-    // pass 2 ------------------------------------------------------------
-    for (int e = tid; e < E; e += SORT_THREADS) {
-        int run = 0;
-        for (int w = 0; w < SORT_WARPS; ++w) {
-            const int c = cnt[w * E + e];
-            cnt[w * E + e] = run;
-            run += c;
+    // 2 ----------------------------------------------------------------------
+    if (warp == 0) {
+        // lane l scans experts [l*per, (l+1)*per); three exclusive scans at once
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per, e1 = min(E, e0 + per);
+        int sp = 0, st = 0, sa = 0;
+        for (int e = e0; e < e1; ++e) {
+            const int n = cnt[e];
+            sp += n;
+            st += (n + NT - 1) / NT;
+            sa += n > 0 ? 1 : 0;
         }
-        etot[e] = run;
-        ecnt[e] = run;
-        etil[e] = (run + NT - 1) / NT;
-        eact[e] = run > 0 ? 1 : 0;
-    }
-    __syncthreads();
-    // three exclusive scans over E (E <= 512): each thread scans a run of
-    // consecutive elements, then the runs' sums are scanned across the block
-    auto block_scan = [&](int32_t* a, int32_t* total) {
-        const int per = (E + SORT_THREADS - 1) / SORT_THREADS;
-        const int b0 = tid * per, b1 = min(E, b0 + per);
-        int v = 0;
-        for (int i = b0; i < b1; ++i) v += a[i];
-        int inc = v;
+        int ip = sp, it = st, ia = sa;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
-            const int o = __shfl_up_sync(0xffffffffu, inc, m);
-            if (lane >= m) inc += o;
-        }
-        if (lane == 31) scan_tmp[warp] = inc;
-        __syncthreads();
-        if (warp == 0) {
-            const int w = lane < SORT_WARPS ? scan_tmp[lane] : 0;
-            int wi = w;
-#pragma unroll
-            for (int m = 1; m < 32; m <<= 1) {
-                const int o = __shfl_up_sync(0xffffffffu, wi, m);
-                if (lane >= m) wi += o;
+            const int a = __shfl_up_sync(0xffffffffu, ip, m);
+            const int b = __shfl_up_sync(0xffffffffu, it, m);
+            const int c = __shfl_up_sync(0xffffffffu, ia, m);
+            if (lane >= m) {
+                ip += a;
+                it += b;
+                ia += c;
             }
-            if (lane < SORT_WARPS) scan_tmp[lane] = wi - w;   // exclusive prefix of the warp sums
-            if (lane == 31) *total = wi;
         }
-        __syncthreads();
-        int run = scan_tmp[warp] + inc - v;
-        for (int i = b0; i < b1; ++i) {
-            const int x = a[i];
-            a[i] = run;
-            run += x;
+        int rp = ip - sp, rt = it - st, ra = ia - sa;   // exclusive prefixes of this lane's run
+        for (int e = e0; e < e1; ++e) {
+            const int n = cnt[e];
+            off[e] = rp;
+            toff[e] = rt;
+            o.counts[e] = n;
+            o.offsets[e] = rp;
+            if (n > 0) o.active[ra++] = e;
+            rp += n;
+            rt += (n + NT - 1) / NT;
         }
-        __syncthreads();
-    };
-    __shared__ int32_t tot_picks, tot_tiles, tot_active;
-    for (int e = tid; e < E; e += SORT_THREADS) counts[e] = ecnt[e];
-    block_scan(etot, &tot_picks);
-    block_scan(etil, &tot_tiles);
-    block_scan(eact, &tot_active);
-    for (int e = tid; e < E; e += SORT_THREADS) {
-        const int n = ecnt[e];
-        offsets[e] = etot[e];
-        if (n > 0) active[eact[e]] = e;
-        for (int i = 0, tb = etil[e]; i * NT < n; ++i) {
-            Tile tl;
-            tl.e = e;
-            tl.p0 = etot[e] + i * NT;
-            tl.n = min(NT, n - i * NT);
-            tl.pad = 0;
-            tiles[tb + i] = tl;
+        if (lane == 31) {
+            off[E] = ip;
+            toff[E] = it;
+            tot_tiles = it;
+            o.offsets[E] = ip;
+            sb->n_picks = ip;
+            sb->n_tiles = it;
+            sb->n_active = ia;
+            sb->work_next = 0;
+            sb->work_next2 = 0;
         }
     }
-    if (tid == 0) {
-        offsets[E] = tot_picks;
-        sb->n_picks = tot_picks;
-        sb->n_tiles = tot_tiles;
-        sb->n_active = tot_active;
-        sb->work_next = 0;
-        sb->work_next2 = 0;
-    }
+    __syncthreads();
 
-    // pass 3 ------------------------------------------------------------
-    const uint32_t lt = (1u << lane) - 1u;
-    for (int g = g0; g < g1; ++g) {
-        const int t = g * 32 + lane;
-        int my[MAX_K];
-        uint32_t valid = 0;
-        if (t < S) {
-            valid = load_ids(t, my);
-#pragma unroll
-            for (int j = 0; j < MAX_K; ++j) {
-                if (valid >> j & 1u) atomicOr(&mask[warp * E + my[j]], 1u << lane);
-                else if (j < k) pos[(size_t)t * k + j] = -1;
-            }
+    // 3 ----------------------------------------------------------------------
+    for (int p = warp * 32 + lane; p < P; p += SORT_THREADS) {
+        const int r = o.pos[p];
+        if (r >= 0) {
+            const int q = off[ids[p]] + r;
+            o.pos[p] = q;
+            o.src[q] = p;
         }
-        __syncwarp();
-        int rank0[MAX_K];
-#pragma unroll
-        for (int j = 0; j < MAX_K; ++j) {
-            rank0[j] = -1;
-            if (valid >> j & 1u) {
-                const int e = my[j];
-                const uint32_t m = mask[warp * E + e];
-                const int r = __popc(m & lt);
-                const int p = etot[e] + cnt[warp * E + e] + r;
-                pos[(size_t)t * k + j] = p;
-                src[p] = t * k + j;
-                rank0[j] = (r == 0) ? __popc(m) : -1;
-            }
-        }
-        __syncwarp();
-#pragma unroll
-        for (int j = 0; j < MAX_K; ++j) {
-            if (rank0[j] >= 0) {
-                const int e = my[j];
-                cnt[warp * E + e] += rank0[j];
-                mask[warp * E + e] = 0u;
-            }
-        }
-        __syncwarp();
     }
+    const int n_tiles = tot_tiles;
+    for (int ti = tid; ti < n_tiles; ti += SORT_THREADS) {
+        // expert of tile ti: the last e with toff[e] <= ti (binary search)
+        int lo = 0, hi = E - 1;
+        while (lo < hi) {
+            const int mid = (lo + hi + 1) >> 1;
+            if (toff[mid] <= ti) lo = mid;
+            else hi = mid - 1;
+        }
+        const int i = ti - toff[lo];
+        Tile tl;
+        tl.e = lo;
+        tl.p0 = off[lo] + i * NT;
+        tl.n = min(NT, cnt[lo] - i * NT);
+        tl.pad = 0;
+        o.tiles[ti] = tl;
+    }
+}
+
+__global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict__ ids, int S, int E, int k,
+                                                       SortOut o) {
+    extern __shared__ int32_t smem[];
+    pdl_trigger();
+    pdl_wait();
+    sort_picks(ids, S, E, k, o, smem);
+}
+
+// moe_forward at small S: the sigmoid top-k of every token (one warp a token,
+// see topk_token) and the sort of its picks in one CTA.  The ids go to the
+// caller's buffer and, for the sort, to shared memory.
+template <int MAXE>
+__global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* __restrict__ L,
+                                                            const float* __restrict__ bias, int S, int E, int k,
+                                                            int32_t* __restrict__ ids,
+                                                            float* __restrict__ weights, SortOut o) {
+    extern __shared__ int32_t smem[];
+    pdl_trigger();
+    pdl_wait();
+    int32_t* sids = smem + sort_smem_ints(E);   // [S][k]
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    for (int t = warp; t < S; t += SORT_THREADS / 32)
+        topk_token<MAXE>(L + (size_t)t * E, bias, E, k, lane, sids + (size_t)t * k, weights + (size_t)t * k);
+    __syncthreads();
+    for (int i = threadIdx.x; i < S * k; i += SORT_THREADS) ids[i] = sids[i];
+    sort_picks(sids, S, E, k, o, smem);
 }
 
 // Token rows of the expert GEMMs.  For every valid pick p < n_picks, token
@@ -212,13 +205,15 @@ __global__ void __launch_bounds__(SORT_WARPS * 32) k_sort(const int32_t* __restr
 // 2^9 below the block maximum (there the error is below 2^-17 of it).  The
 // unused bytes of the last stage's scale rows of xs and hs (K / 32 not a
 // multiple of 8) are set to 127 (scale 1), as their codes are zero.
-// grid (max_picks), 128 threads; a thread takes 8 elements, four threads a
-// block.
-__global__ void __launch_bounds__(128) k_quant_gather(const __nv_bfloat16* __restrict__ x,
+// grid (max_picks), blockDim = d / 8 rounded up to a warp (at most 1024): a
+// thread takes 8 elements, four threads a block, in one pass for d <= 8192.
+__global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __restrict__ x,
                                                       const int32_t* __restrict__ src, int k, int d, int I, int P,
                                                       uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
                                                       uint8_t* __restrict__ hs,
                                                       const StatusBlock* __restrict__ sb) {
+    pdl_trigger();
+    pdl_wait();
     const int p = blockIdx.x;
     const int sp = src[p];                 // read beside n_picks: src has max_picks entries
     if (p >= sb->n_picks) return;
@@ -276,34 +271,59 @@ __global__ void __launch_bounds__(128) k_quant_gather(const __nv_bfloat16* __res
 
 }  // namespace
 
-cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+static SortOut sort_out(const WsLayout& L, char* ws) {
+    SortOut o;
+    o.counts = reinterpret_cast<int32_t*>(ws + L.counts);
+    o.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
+    o.pos = reinterpret_cast<int32_t*>(ws + L.pos);
+    o.src = reinterpret_cast<int32_t*>(ws + L.src);
+    o.tiles = reinterpret_cast<Tile*>(ws + L.tiles);
+    o.active = reinterpret_cast<int32_t*>(ws + L.active);
+    o.tile_ready = reinterpret_cast<uint32_t*>(ws + L.tile_ready);
+    o.max_tiles = L.max_tiles;
+    o.sb = reinterpret_cast<StatusBlock*>(ws + L.status);
+    return o;
+}
+
+static cudaError_t launch_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     char* ws = p.ws;
-    StatusBlock* sb = reinterpret_cast<StatusBlock*>(ws + L.status);
-    // small batches: 8 warps (the per-warp tables are then 8 x E); large: 32
-    const bool big = (size_t)s.S * s.k > 2048;
-    const int warps = big ? 32 : 8;
-    const size_t smem = (size_t)(2 * warps * s.E + 4 * s.E) * sizeof(int32_t);
-    auto kern = big ? k_sort<32> : k_sort<8>;
+    timing_begin(K_GATHER, st);
+    const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
+    const cudaError_t e = launch_pdl(k_quant_gather, dim3(L.max_picks), dim3(threads), 0, st, p.x,
+                                     reinterpret_cast<const int32_t*>(ws + L.src), s.k, s.d, s.I, L.max_picks,
+                                     reinterpret_cast<uint8_t*>(ws + L.xq), reinterpret_cast<uint8_t*>(ws + L.xs),
+                                     reinterpret_cast<uint8_t*>(ws + L.hs),
+                                     reinterpret_cast<const StatusBlock*>(ws + L.status));
+    timing_end(st);
+    return e;
+}
+
+cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    const size_t smem = (size_t)sort_smem_ints(s.E) * sizeof(int32_t);
+    timing_begin(K_SORT, st);
+    cudaError_t e = launch_pdl(k_sort, dim3(1), dim3(SORT_THREADS), smem, st, (const int32_t*)p.ids, s.S, s.E, s.k,
+                               sort_out(L, p.ws));
+    timing_end(st);
+    if (e != cudaSuccess) return e;
+    return launch_gather(s, L, p, st);
+}
+
+bool topk_sort_fits(const moe_shape& s) {
+    // at most 4 tokens a warp, and the ids of the call in shared memory
+    return s.S <= 4 * (SORT_THREADS / 32) && (size_t)s.S * s.k <= 8192;
+}
+
+cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    const size_t smem = ((size_t)sort_smem_ints(s.E) + (size_t)s.S * s.k) * sizeof(int32_t);
+    auto kern = s.E <= 256 ? k_topk_sort<256 / 32> : k_topk_sort<512 / 32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    timing_begin(K_SORT, st);
-    kern<<<1, warps * 32, smem, st>>>(p.ids, s.S, s.E, s.k, reinterpret_cast<int32_t*>(ws + L.counts),
-                                          reinterpret_cast<int32_t*>(ws + L.offsets),
-                                          reinterpret_cast<int32_t*>(ws + L.pos),
-                                          reinterpret_cast<int32_t*>(ws + L.src),
-                                          reinterpret_cast<Tile*>(ws + L.tiles),
-                                          reinterpret_cast<int32_t*>(ws + L.active),
-                                          reinterpret_cast<uint32_t*>(ws + L.tile_ready), L.max_tiles, sb);
+    timing_begin(K_TOPK_SORT, st);
+    e = launch_pdl(kern, dim3(1), dim3(SORT_THREADS), smem, st, reinterpret_cast<const float*>(p.ws + L.logits),
+                   p.bias, s.S, s.E, s.k, p.ids, p.weights, sort_out(L, p.ws));
     timing_end(st);
-    e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    timing_begin(K_GATHER, st);
-    k_quant_gather<<<L.max_picks, 128, 0, st>>>(p.x, reinterpret_cast<const int32_t*>(ws + L.src), s.k, s.d, s.I,
-                                                L.max_picks, reinterpret_cast<uint8_t*>(ws + L.xq),
-                                                reinterpret_cast<uint8_t*>(ws + L.xs),
-                                                reinterpret_cast<uint8_t*>(ws + L.hs), sb);
-    timing_end(st);
-    return cudaGetLastError();
+    return launch_gather(s, L, p, st);
 }
 
 }  // namespace moe

@@ -17,7 +17,7 @@ std::vector<Rec> g_recs;   // event pairs, created by moe_timing_enable
 int g_used = 0;            // pairs recorded since the last collect
 int g_open = -1;           // pair started by timing_begin, not yet ended
 
-const char* const kNames[K_NUM] = {"router_logits", "topk", "sort", "gather", "experts", "combine"};
+const char* const kNames[K_NUM] = {"router_logits", "topk", "sort", "gather", "experts", "combine", "topk_sort"};
 
 void free_all() {
     for (auto& r : g_recs) {
