@@ -63,20 +63,15 @@ namespace {
 
 constexpr int KS = 256;                      // K elements of one stage
 constexpr int AROWS = 128;                   // MMA M
-constexpr int NB = 2 * NT;                   // MMA N: a hi and a lo row per pick
 constexpr int A_SLAB = AROWS * 128;          // one 128-K slab of the weight tile in shared memory (unpacked)
 constexpr int A_SMEM = 2 * A_SLAB;           // 32 KB
 constexpr int A_TX = AROWS * KS / 2;         // packed bytes of a weight tile: the TMA transaction count
-constexpr int B_SLAB = NB * 128;             // one 128-K slab of the token tile
-constexpr int B_SMEM = 2 * B_SLAB;           // 8 KB
-constexpr int BS_BYTES = NT * TOKEN_SCALE_ROW;   // the tile's token scale rows
 #ifndef MOE_MX_TOKEN_STAGES
 #define MOE_MX_TOKEN_STAGES 4
 #endif
 constexpr int NSB = MOE_MX_TOKEN_STAGES;     // token-tile stages
 constexpr int TMEM_COLS = 512;
 constexpr int NMMA = 2;                      // MMA-issuing warps (one thread each)
-constexpr int SF_COL0 = 2 * NMMA * NB;       // TMEM columns of the scale slots (after the accumulators)
 // One stage's scale slot in TMEM, 64 columns: the weight scales of K steps
 // 0-3 at +0 and of K steps 4-7 at +16 (row m of the tile in lane m, column
 // + m / 32), the token scales at +32 and +48 (column n in lane n of every lane
@@ -92,17 +87,25 @@ constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 // STMA: the e8m0 bytes of the weights come by TMA, 16 bytes (512 K) of each
 // row per stage, when the scale rows are 16-byte aligned (K % 512 == 0);
 // otherwise by 4-byte cp.async, 8 bytes (256 K) of each row per stage.
-template <bool STMA>
+// NTT: picks per tile (8 or 16); the MMA N is 2 NTT.
+template <bool STMA, int NTT>
 struct Cfg {
+    static constexpr int NB = 2 * NTT;                         // MMA N: a hi and a lo row per pick
+    static constexpr int B_SLAB = NB * 128;                    // one 128-K slab of the token tile
+    static constexpr int B_SMEM = 2 * B_SLAB;                  // a token stage (4 or 8 KB)
+    static constexpr int BS_BYTES = NTT * TOKEN_SCALE_ROW;     // the tile's token scale rows
+    static constexpr int SF_COL0 = 2 * NMMA * NB;              // TMEM columns of the scale slots
+
     static constexpr int SC_ROW = STMA ? 16 : 8;               // e8m0 bytes of a row in a stage
     static constexpr int SC_BYTES = AROWS * SC_ROW;
     static constexpr int SC_OFF = A_SMEM;                      // within a weight stage
     static constexpr int A_STAGE = (A_SMEM + SC_BYTES + 1023) / 1024 * 1024;
-    static constexpr int B_STAGE = (B_SMEM + BS_BYTES + 1023) / 1024 * 1024;
-    static constexpr int XCH_STRIDE = NT + 1;
+    static constexpr int B_STAGE = B_SMEM;                     // the token scale rows sit apart
+    static constexpr int XCH_STRIDE = NTT + 1;
     static constexpr int XCH_BYTES = 64 * XCH_STRIDE * 4;
     static constexpr int RING_BYTES = UR * 32;
-    static constexpr int MISC = 1024 /*align slack*/ + XCH_BYTES + RING_BYTES + 1024 /*barriers*/;
+    static constexpr int TSC_BYTES = NSB * BS_BYTES;
+    static constexpr int MISC = 1024 /*align slack*/ + XCH_BYTES + RING_BYTES + TSC_BYTES + 1024 /*barriers*/;
     static constexpr int NSA_FIT = (232448 - MISC - NSB * B_STAGE) / A_STAGE;
     static constexpr int NSA_TMEM = (TMEM_COLS - SF_COL0) / SF_SLOT;
     static constexpr int NSA = NSA_FIT < NSA_TMEM ? NSA_FIT : NSA_TMEM;
@@ -118,11 +121,11 @@ struct Args {
     const uint8_t* w13s;
     const uint8_t* w2s;
     uint8_t* hq;          // [2P][I] e4m3: row 2p = hi, row 2p + 1 = lo of pick p's h
-    uint8_t* hs;          // [ceil(I/256)][P + NT][16] e8m0 block scales of h
+    uint8_t* hs;          // [ceil(I/256)][P + NT_MAX][16] e8m0 block scales of h
     float* y;
     float* ssq;           // per-pick sums of y^2 by 128-row block, or null
     uint32_t* tile_ready;
-    const uint8_t* xs;    // [ceil(d/256)][P + NT][16] e8m0 block scales of the gathered tokens
+    const uint8_t* xs;    // [ceil(d/256)][P + NT_MAX][16] e8m0 block scales of the gathered tokens
     int d, I, P;
 };
 
@@ -158,20 +161,22 @@ __device__ __forceinline__ int weight_row(const Unit& U, int r, const Args& a) {
     return U.e * a.d + U.mb * AROWS + r;
 }
 
-template <bool STMA>
+template <bool STMA, int NTT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_experts_mx(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
                  const __grid_constant__ CUtensorMap tm_xq, const __grid_constant__ CUtensorMap tm_hq,
                  const __grid_constant__ CUtensorMap tm_w13s, const __grid_constant__ CUtensorMap tm_w2s,
                  const Args a) {
-    using C = Cfg<STMA>;
-    constexpr int NSA = C::NSA;
+    using C = Cfg<STMA, NTT>;
+    constexpr int NSA = C::NSA, NB = C::NB, B_SLAB = C::B_SLAB, B_SMEM = C::B_SMEM, BS_BYTES = C::BS_BYTES;
+    constexpr int SF_COL0 = C::SF_COL0;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* wst = smem;                                  // weight stages [NSA][A_STAGE]
     uint8_t* tst = smem + NSA * C::A_STAGE;               // token stages [NSB][B_STAGE]
     float* xch = reinterpret_cast<float*>(tst + NSB * C::B_STAGE);
-    Unit* uring = reinterpret_cast<Unit*>(reinterpret_cast<uint8_t*>(xch) + C::XCH_BYTES);
+    uint8_t* tsc = reinterpret_cast<uint8_t*>(xch) + C::XCH_BYTES;   // token scale rows [NSB][BS_BYTES]
+    Unit* uring = reinterpret_cast<Unit*>(tsc + C::TSC_BYTES);
     uint64_t* bars = reinterpret_cast<uint64_t*>(reinterpret_cast<uint8_t*>(uring) + C::RING_BYTES);
     uint64_t* full_a = bars;                // [NSA] weight tile + its scales landed
     uint64_t* empty_a = full_a + NSA;       // [NSA] both issuers done with the weight stage
@@ -345,7 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == TOK_WARP) {
         // ------------------------------------------------------------ token producer
         const uint64_t pol_x = ptx::policy_evict_last();
-        const size_t tab_rows = (size_t)a.P + NT;
+        const size_t tab_rows = (size_t)a.P + NT_MAX;
         int ts = 0;
         bool ok = true;
         for (int i = 0; ok; ++i) {
@@ -387,8 +392,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     uint8_t* st = tst + s * C::B_STAGE;
                     ptx::mbar_arrive_expect_tx(&full_b[s], B_SMEM + BS_BYTES);
                     ptx::tma_load_3d(st, tmB, 0, 2 * U.p0, 2 * c, &full_b[s], pol_x);
-                    ptx::bulk_load(st + B_SMEM, tab + ((size_t)c * tab_rows + U.p0) * TOKEN_SCALE_ROW, BS_BYTES,
-                                   &full_b[s], pol_x);
+                    ptx::bulk_load(tsc + s * BS_BYTES, tab + ((size_t)c * tab_rows + U.p0) * TOKEN_SCALE_ROW,
+                                   BS_BYTES, &full_b[s], pol_x);
                 }
                 __syncwarp();
             }
@@ -417,7 +422,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 const uint8_t* st = wst + s * C::A_STAGE;
                 const uint2 wa = *reinterpret_cast<const uint2*>(st + C::SC_OFF + C::SC_ROW * r + (STMA ? 8 * (c & 1) : 0));
-                const uint2 wb = *reinterpret_cast<const uint2*>(tst + sbi * C::B_STAGE + B_SMEM + TOKEN_SCALE_ROW * (lane >> 1));
+                // token column n = lane: pick lane / 2 (hi and lo row); lanes past the
+                // tile's 2 NTT columns are never read
+                const uint2 wb = *reinterpret_cast<const uint2*>(
+                    tsc + sbi * BS_BYTES + TOKEN_SCALE_ROW * ((lane >> 1) & (NTT - 1)));
                 // 0xFF is NaN in e8m0
                 const uint32_t nan_a = __vcmpeq4(wa.x, 0xFFFFFFFFu) | __vcmpeq4(wa.y, 0xFFFFFFFFu);
                 if (nan_a) latch_status(sb, MOE_ERR_BAD_SCALE, 255);
@@ -503,7 +511,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int qd = warp & 3;
         const int r = 32 * qd + lane;
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
-        const size_t tab_rows = (size_t)a.P + NT;
+        const size_t tab_rows = (size_t)a.P + NT_MAX;
         for (int i = 0;; ++i) {
             const int ab = i & 1;
             // the four epilogue warps take one decision before their named
@@ -522,9 +530,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (*epi_flag || end) break;
             ptx::tc_fence_after();
             // v[n]: the issuers' stages, hi + lo column of pick n
-            float v[NT];
+            float v[NTT];
 #pragma unroll
-            for (int n = 0; n < NT; ++n) v[n] = 0.f;
+            for (int n = 0; n < NTT; ++n) v[n] = 0.f;
             const int n_iss = U.stages < NMMA ? U.stages : NMMA;   // issuers that had a stage
 #pragma unroll
             for (int mm = 0; mm < NMMA; ++mm) {
@@ -535,7 +543,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ptx::tmem_ld16(tmem + lane_base + (ab * NMMA + mm) * NB + 16 * j, t + 16 * j);
                 ptx::tmem_ld_wait();
 #pragma unroll
-                for (int n = 0; n < NT; ++n) v[n] += __uint_as_float(t[2 * n]) + __uint_as_float(t[2 * n + 1]);
+                for (int n = 0; n < NTT; ++n) v[n] += __uint_as_float(t[2 * n]) + __uint_as_float(t[2 * n + 1]);
             }
             ptx::tc_fence_before();
             __syncwarp();
@@ -544,22 +552,22 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // lanes 0..63: gate of rows mb*64 + r; lanes 64..127: up of the same rows
                 if (r >= 64) {
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) xch[(r - 64) * C::XCH_STRIDE + n] = v[n];
+                    for (int n = 0; n < NTT; ++n) xch[(r - 64) * C::XCH_STRIDE + n] = v[n];
                 }
                 ptx::named_bar_sync(1, 128);
                 if (r < 64) {
                     // warp qd (0 or 1) holds the 32 rows of h block mb*2 + qd
                     const int ii = U.mb * 64 + r;
                     const int blk = ii / 32;
-                    float h[NT];
+                    float h[NTT];
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) {
+                    for (int n = 0; n < NTT; ++n) {
                         const float gv = v[n];
                         const float uv = xch[r * C::XCH_STRIDE + n];
                         h[n] = n < U.n ? gv / (1.0f + __expf(-gv)) * uv : 0.f;
                     }
 #pragma unroll
-                    for (int n = 0; n < NT; n += 2) {
+                    for (int n = 0; n < NTT; n += 2) {
                         uint32_t byte2[2];
                         float hs2[2];
 #pragma unroll
@@ -596,20 +604,20 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             } else {
                 const int m = U.mb * AROWS + r;
 #pragma unroll
-                for (int n = 0; n < NT; ++n)
+                for (int n = 0; n < NTT; ++n)
                     if (n < U.n) a.y[(size_t)(U.p0 + n) * a.d + m] = v[n];
                 if (a.ssq != nullptr) {
                     // sum of y^2 over the unit's 128 rows for every pick: a
                     // reduce-scatter across the warp (lane l ends with pick idx),
                     // then the four warps' sums in warp order
-                    float q[NT];
+                    float q[NTT];
 #pragma unroll
-                    for (int n = 0; n < NT; ++n) q[n] = v[n] * v[n];
+                    for (int n = 0; n < NTT; ++n) q[n] = v[n] * v[n];
                     int idx = 0;
 #pragma unroll
                     for (int step = 0; step < 5; ++step) {
                         const int o = 16 >> step;
-                        const int c = NT >> step;       // values a lane holds before this step
+                        const int c = NTT >> step;      // values a lane holds before this step
                         const bool hi = (lane & o) != 0;
                         if (c > 1) {
 #pragma unroll
@@ -623,13 +631,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                             q[0] += __shfl_xor_sync(0xffffffffu, q[0], o);
                         }
                     }
-                    static_assert(NT == 16, "the reduce-scatter leaves one pick on every lane pair");
-                    float* part = xch;                             // [4][NT]
-                    if ((lane & 1) == 0) part[qd * NT + idx] = q[0];
+                    // every pick's sum now sits on 32 / NTT lanes
+                    float* part = xch;                             // [4][NTT]
+                    if ((lane & (32 / NTT - 1)) == 0) part[qd * NTT + idx] = q[0];
                     ptx::named_bar_sync(1, 128);
                     if (r < U.n)
                         a.ssq[(size_t)(U.p0 + r) * (a.d / AROWS) + U.mb] =
-                            ((part[r] + part[NT + r]) + part[2 * NT + r]) + part[3 * NT + r];
+                            ((part[r] + part[NTT + r]) + part[2 * NTT + r]) + part[3 * NTT + r];
                 }
             }
         }
@@ -688,9 +696,9 @@ int num_sms() {
     return n[dev];
 }
 
-template <bool STMA>
+template <bool STMA, int NTT>
 cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    using C = Cfg<STMA>;
+    using C = Cfg<STMA, NTT>;
     CUtensorMap tm_w13, tm_w2, tm_xq, tm_hq, tm_w13s, tm_w2s;
     const uint64_t P = (uint64_t)L.max_picks, E = s.E, d = s.d, I = s.I;
     const CUtensorMapDataType U8 = CU_TENSOR_MAP_DATA_TYPE_UINT8, U4 = CU_TENSOR_MAP_DATA_TYPE_16U4_ALIGN16B;
@@ -703,7 +711,7 @@ cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
     // xq [2P][d] / hq [2P][I] e4m3 as {128 bytes, 2P rows, K/128 slabs}
     const uint64_t xq_d[3] = {128, 2 * P, d / 128}, xq_s[2] = {d, 128};
     const uint64_t hq_d[3] = {128, 2 * P, I / 128}, hq_s[2] = {I, 128};
-    const uint32_t tok_b[3] = {128, (uint32_t)NB, 2};
+    const uint32_t tok_b[3] = {128, (uint32_t)C::NB, 2};
     if (!make_map(&tm_w13, U4, p.w13, 4, w13_d, w13_s, w13_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_w2, U4, p.w2, 3, w2_d, w2_s, w2_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
         !make_map(&tm_xq, U8, p.ws + L.xq, 3, xq_d, xq_s, tok_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
@@ -722,7 +730,7 @@ cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
         tm_w13s = tm_w13;   // unused
         tm_w2s = tm_w2;
     }
-    cudaError_t e = cudaFuncSetAttribute(k_experts_mx<STMA>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_experts_mx<STMA, NTT>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     Args a;
     a.tiles = reinterpret_cast<const Tile*>(p.ws + L.tiles);
@@ -738,7 +746,7 @@ cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
     a.d = s.d;
     a.I = s.I;
     a.P = L.max_picks;
-    return launch_pdl(k_experts_mx<STMA>, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, tm_w13, tm_w2, tm_xq, tm_hq,
+    return launch_pdl(k_experts_mx<STMA, NTT>, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, tm_w13, tm_w2, tm_xq, tm_hq,
                       tm_w13s, tm_w2s, a);
 }
 
@@ -747,7 +755,11 @@ cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     timing_begin(K_EXPERTS, st);
     const bool stma = (s.d % 512 == 0) && (s.I % 512 == 0);
-    cudaError_t e = stma ? launch_mx<true>(s, L, p, st) : launch_mx<false>(s, L, p, st);
+    cudaError_t e;
+    if (L.nt == 8)
+        e = stma ? launch_mx<true, 8>(s, L, p, st) : launch_mx<false, 8>(s, L, p, st);
+    else
+        e = stma ? launch_mx<true, 16>(s, L, p, st) : launch_mx<false, 16>(s, L, p, st);
     timing_end(st);
     return e;
 }

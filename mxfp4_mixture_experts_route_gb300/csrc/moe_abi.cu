@@ -9,12 +9,20 @@ namespace moe {
 
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
+// Picks per expert tile: 8 while the average expert gets at most 2 picks (the
+// tile then carries little padding, and the expert kernel's smaller token
+// stages leave room for one more weight stage), else 16 (with more picks per
+// expert a second tile, which reads the expert's weights again, gets likely).
+int tile_picks(const moe_shape& s) { return (int64_t)s.S * s.k <= 2 * (int64_t)s.E ? 8 : 16; }
+
 WsLayout ws_layout(const moe_shape& s) {
     WsLayout L{};
     const size_t P = (size_t)s.S * s.k;                  // picks
     L.max_picks = (int)P;
-    // sum_e ceil(n_e / NT) <= P / NT + (experts with a pick) <= ceil(P / NT) + min(E, P)
-    L.max_tiles = (int)((P + NT - 1) / NT + (P < (size_t)s.E ? P : (size_t)s.E));
+    L.nt = tile_picks(s);
+    const size_t nt = (size_t)L.nt;
+    // sum_e ceil(n_e / nt) <= P / nt + (experts with a pick) <= ceil(P / nt) + min(E, P)
+    L.max_tiles = (int)((P + nt - 1) / nt + (P < (size_t)s.E ? P : (size_t)s.E));
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(sizeof(StatusBlock));
@@ -30,7 +38,7 @@ WsLayout ws_layout(const moe_shape& s) {
     L.active = take((size_t)s.E * 4);
     L.tile_ready = take((size_t)L.max_tiles * 4);
     // e4m3 hi / lo rows of the gathered tokens and of h, and their block scales
-    const size_t rows = P + NT;
+    const size_t rows = P + NT_MAX;
     L.xq = take(2 * P * s.d);
     L.xs = take((size_t)((s.d + 255) / 256) * rows * TOKEN_SCALE_ROW);
     L.hq = take(2 * P * s.I);

@@ -27,18 +27,20 @@ struct StatusBlock {
 };
 static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
 
-// Token-tile width of the expert GEMMs: one tile holds up to NT picks of one
-// expert (the MMA N dimension; the pages' 16-row tiles, k5 page).
-constexpr int NT = 16;
+// Token-tile width of the expert GEMMs: one tile holds up to nt picks of one
+// expert (an MMA N of 2 nt: hi and lo row per pick), nt = 16 (the pages'
+// 16-row tiles, k5 page) or 8 when the calls' experts get few picks each.
+constexpr int NT_MAX = 16;
+int tile_picks(const moe_shape& s);
 
 // Block scales of the gathered tokens and of h (e8m0, one per 32 elements):
 // a table [ceil(K/256) stages][P + NT picks][TOKEN_SCALE_ROW bytes], bytes
 // 0..7 of a row holding the stage's eight scales (16-byte rows, so that the
-// 16 rows of a tile are one aligned bulk copy; NT rows of padding so that the
-// last tile's copy stays inside the table).
+// rows of a tile are one aligned bulk copy; NT_MAX rows of padding so that
+// the last tile's copy stays inside the table).
 constexpr int TOKEN_SCALE_ROW = 16;
 
-// One work tile: expert e, first sorted pick p0, n picks (n <= NT).
+// One work tile: expert e, first sorted pick p0, n picks (n <= nt).
 struct Tile {
     int32_t e, p0, n, pad;
 };
@@ -49,6 +51,7 @@ struct WsLayout {
     size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
     size_t total;
     int max_tiles;
+    int nt;               // picks per tile (8 or 16)
     int max_picks;
     int router_kslices;   // K-ranges of the router (CTAs of one cluster)
 };

@@ -4,7 +4,7 @@
 // operands ... expert etab[u], u clamped below nv" -- the pages keep a table of
 // the local experts that have picks and run tasks (expert, tile).  Here that
 // table is built once per call: picks are counted per expert, placed in one
-// segment per expert, and each segment is cut into tiles of at most NT picks
+// segment per expert, and each segment is cut into tiles of at most nt picks
 // (k5 page: "Every row tile is 16 tokens").  Experts without picks get no
 // tile, so no weight byte of an untouched expert is read.
 #include "moe_internal.cuh"
@@ -28,6 +28,7 @@ struct SortOut {
     int32_t* active;
     uint32_t* tile_ready;
     int max_tiles;
+    int nt;               // picks per tile
     StatusBlock* sb;
 };
 
@@ -56,6 +57,7 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
     __shared__ int32_t tot_tiles;
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = S * k;
+    const int nt = o.nt;
     StatusBlock* sb = o.sb;
 
     for (int i = tid; i <= E; i += SORT_THREADS) cnt[i] = 0;
@@ -100,7 +102,7 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
         for (int e = e0; e < e1; ++e) {
             const int n = cnt[e];
             sp += n;
-            st += (n + NT - 1) / NT;
+            st += (n + nt - 1) / nt;
             sa += n > 0 ? 1 : 0;
         }
         int ip = sp, it = st, ia = sa;
@@ -124,7 +126,7 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
             o.offsets[e] = rp;
             if (n > 0) o.active[ra++] = e;
             rp += n;
-            rt += (n + NT - 1) / NT;
+            rt += (n + nt - 1) / nt;
         }
         if (lane == 31) {
             off[E] = ip;
@@ -161,8 +163,8 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
         const int i = ti - toff[lo];
         Tile tl;
         tl.e = lo;
-        tl.p0 = off[lo] + i * NT;
-        tl.n = min(NT, cnt[lo] - i * NT);
+        tl.p0 = off[lo] + i * nt;
+        tl.n = min(nt, cnt[lo] - i * nt);
         tl.pad = 0;
         o.tiles[ti] = tl;
     }
@@ -218,7 +220,7 @@ __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __re
     const int sp = src[p];                 // read beside n_picks: src has max_picks entries
     if (p >= sb->n_picks) return;
     const int t = sp / k;
-    const size_t rows = (size_t)P + NT;
+    const size_t rows = (size_t)P + NT_MAX;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     uint8_t* hi_row = xq + (size_t)(2 * p) * d;
     uint8_t* lo_row = hi_row + d;
@@ -281,6 +283,7 @@ static SortOut sort_out(const WsLayout& L, char* ws) {
     o.active = reinterpret_cast<int32_t*>(ws + L.active);
     o.tile_ready = reinterpret_cast<uint32_t*>(ws + L.tile_ready);
     o.max_tiles = L.max_tiles;
+    o.nt = L.nt;
     o.sb = reinterpret_cast<StatusBlock*>(ws + L.status);
     return o;
 }
