@@ -162,9 +162,18 @@ def algorithmic_bytes(cfg: mi.MoEConfig, n_touched: int) -> dict:
     }
 
 
+# the sources a kernel is compiled from (its profile goes stale when one changes)
+KERNEL_SOURCES = {
+    "experts": ["experts_mx.cu", "tc_ptx.cuh", "moe_internal.cuh"],
+}
+
+
 def kernel_source_sha(name: str) -> str:
     h = hashlib.sha256()
-    for p in sorted(glob.glob(os.path.join(ROOT, "mxfp4_mixture_experts_route_gb300", "csrc", "*"))):
+    csrc = os.path.join(ROOT, "mxfp4_mixture_experts_route_gb300", "csrc")
+    files = KERNEL_SOURCES.get(name)
+    paths = [os.path.join(csrc, f) for f in files] if files else sorted(glob.glob(os.path.join(csrc, "*")))
+    for p in paths:
         h.update(open(p, "rb").read())
     return h.hexdigest()[:12]
 
@@ -375,8 +384,9 @@ def run_ours(args, cfg: mi.MoEConfig):
         dist.destroy_process_group()
 
 
-# arithmetic type of the expert path: bf16 tensor-core MMA (fp32 accumulate)
-DTYPE = "bf16"
+# arithmetic type of the expert path: block-scaled tensor-core MMA of e2m1
+# weights and e4m3 token halves, fp32 accumulation (router: bf16 x bf16, fp32)
+DTYPE = "e2m1xe4m3"
 
 
 def main():
