@@ -25,8 +25,7 @@
 // epilogue adds each pick's two columns.
 //
 // One persistent CTA per SM, 12 warps:
-//   warp 0      weight producer: claims the CTA's next unit, and per 256-K
-//               stage of a unit loads the weight tile (128 rows x 256 K e2m1 =
+//   warp 0      weight producer: per 256-K stage of a unit, the weight tile (128 rows x 256 K e2m1 =
 //               16 KB of HBM, 32 KB unpacked in shared memory; gate and up rows
 //               in one 4-D box) and its e8m0 bytes into a ring of weight stages.
 //   warp 7      token producer: the token tile (32 e4m3 rows x 256 K, one 3-D
@@ -35,6 +34,9 @@
 //               down unit it first waits (bounded) for the tile's h.
 //   warps 8-11  scale movers: copy the stage's weight and token block scales
 //               from shared memory into TMEM, in the layout the MMA reads.
+//   warp 12     unit scheduler: claims units and reads their tile entries
+//               (global-memory round trips) at most LOOKAHEAD units ahead of the
+//               weight producer, and publishes them in the CTA's unit ring.
 //   warps 1-2   MMA issuers (lane 0 of each): M = 128 weight rows, N = 32,
 //               K = 32; issuer m takes the stages of parity m of every unit
 //               into an fp32 accumulator of its own (double buffered by unit).
@@ -45,8 +47,9 @@
 //               column added; h = silu(g) * u split into e4m3 hi/lo rows with a
 //               block scale per 32 rows for gate_up; y (fp32) and per-128-row
 //               sums of squares for down.
-// Work units, claimed by the CTAs from a device-wide counter (reset by the
-// sort kernel) so that a CTA that finishes early takes more: gate_up units
+// Work units: CTA b starts with unit b and claims the next ones from a
+// device-wide counter (reset by the sort kernel), so that a CTA that finishes
+// early takes more.  Gate_up units
 // first (64 gate rows stacked on the matching 64 up rows = one M = 128
 // operand), then down units (128 rows of w2).  A down unit needs the h rows of
 // its tile: the counter of the tile, which every finished gate_up unit of it
@@ -78,8 +81,9 @@ constexpr int NMMA = 2;                      // MMA-issuing warps (one thread ea
 // quarter).  Every scale address the MMA gets is a multiple of 16 columns.
 constexpr int SF_SLOT = 64;
 constexpr int SF_A1 = 16, SF_B0 = 32, SF_B1 = 48;
-constexpr int MMA_WARP0 = 1, EPI_WARP0 = 3, TOK_WARP = 7, SF_WARP0 = 8;
-constexpr int NUM_WARPS = 12;
+constexpr int MMA_WARP0 = 1, EPI_WARP0 = 3, TOK_WARP = 7, SF_WARP0 = 8, SCHED_WARP = 12;
+constexpr int NUM_WARPS = 13;
+constexpr int LOOKAHEAD = 2;                 // units the scheduler publishes ahead of the weight producer
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 constexpr int UR = 32;                       // unit ring entries
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
@@ -94,7 +98,11 @@ struct Cfg {
     static constexpr int B_SLAB = NB * 128;                    // one 128-K slab of the token tile
     static constexpr int B_SMEM = 2 * B_SLAB;                  // a token stage (4 or 8 KB)
     static constexpr int BS_BYTES = NTT * TOKEN_SCALE_ROW;     // the tile's token scale rows
-    static constexpr int SF_COL0 = 2 * NMMA * NB;              // TMEM columns of the scale slots
+    // fp32 accumulators: ACCB buffers (by unit) x NMMA issuers x NB columns; 4
+    // buffers when they fit beside six scale slots, so that short units do not
+    // wait for the epilogue to drain the buffer of two units back
+    static constexpr int ACCB = NTT == 8 ? 4 : 2;
+    static constexpr int SF_COL0 = ACCB * NMMA * NB;           // TMEM columns of the scale slots
 
     static constexpr int SC_ROW = STMA ? 16 : 8;               // e8m0 bytes of a row in a stage
     static constexpr int SC_BYTES = AROWS * SC_ROW;
@@ -127,6 +135,7 @@ struct Args {
     uint32_t* tile_ready;
     const uint8_t* xs;    // [ceil(d/256)][P + NT_MAX][16] e8m0 block scales of the gathered tokens
     int d, I, P;
+    int max_tiles;
 };
 
 struct Unit {
@@ -169,7 +178,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  const Args a) {
     using C = Cfg<STMA, NTT>;
     constexpr int NSA = C::NSA, NB = C::NB, B_SLAB = C::B_SLAB, B_SMEM = C::B_SMEM, BS_BYTES = C::BS_BYTES;
-    constexpr int SF_COL0 = C::SF_COL0;
+    constexpr int SF_COL0 = C::SF_COL0, ACCB = C::ACCB;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* wst = smem;                                  // weight stages [NSA][A_STAGE]
@@ -183,14 +192,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* full_b = empty_a + NSA;       // [NSB] token tile + its scales landed
     uint64_t* empty_b = full_b + NSB;       // [NSB] both issuers done with the token stage
     uint64_t* sf_full = empty_b + NSB;      // [NSA] the stage's scales are in TMEM
-    uint64_t* acc_full = sf_full + NSA;     // [2]
-    uint64_t* acc_empty = acc_full + 2;     // [2]
-    uint64_t* u_full = acc_empty + 2;       // [UR]
+    uint64_t* acc_full = sf_full + NSA;     // [ACCB]
+    uint64_t* acc_empty = acc_full + ACCB;  // [ACCB]
+    uint64_t* u_full = acc_empty + ACCB;    // [UR]
     uint64_t* u_empty = u_full + UR;        // [UR]
     uint64_t* fin = u_empty + UR;           // [NMMA]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + NMMA);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* epi_flag = abort_flag + 1;
+    volatile int* taken = abort_flag + 2;   // units the weight producer has taken
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     StatusBlock* sb = a.sb;
@@ -206,16 +216,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_init(&full_b[i], 1);
             ptx::mbar_init(&empty_b[i], 1);
         }
-        for (int i = 0; i < 2; ++i) {
+        for (int i = 0; i < ACCB; ++i) {
             ptx::mbar_init(&acc_full[i], NMMA);
             ptx::mbar_init(&acc_empty[i], 4);
         }
         for (int i = 0; i < UR; ++i) {
             ptx::mbar_init(&u_full[i], 1);
-            ptx::mbar_init(&u_empty[i], NMMA + 1 + 4 + 4);   // MMA, token producer, scale movers, epilogue
+            ptx::mbar_init(&u_empty[i], NMMA + 1 + 4 + 4 + 1);   // MMA, token, scale movers, epilogue, weights
         }
         for (int i = 0; i < NMMA; ++i) ptx::mbar_init(&fin[i], 1);
         *abort_flag = 0;
+        *taken = 0;
         ptx::fence_mbar_init();
     }
     if (warp == MMA_WARP0) ptx::tmem_alloc(tmem_holder, TMEM_COLS);
@@ -234,14 +245,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the set-up above needs nothing from the preceding kernels; everything
     // below reads their results
     pdl_wait();
-    // the weight producer's first two unit claims and the tile count
-    int claim0 = 0, claim1 = 0, n_tiles = 0;
-    if (warp == 0) {
+    // CTA b's first unit is unit b; the later ones are claimed from the counter
+    // (offset by the grid size).  The tile count, the first unit's tile entry
+    // (read as if it were a gate_up unit, the usual case, and read again below
+    // if not) and the second claim are all in flight at once.
+    int claim1 = 0, n_tiles = 0;
+    Tile tile0 = {0, 0, 0, 0};
+    if (warp == SCHED_WARP) {
         n_tiles = sb->n_tiles;
-        if (lane == 0) {
-            claim0 = atomicAdd(&sb->work_next, 1);
-            claim1 = atomicAdd(&sb->work_next, 1);
-        }
+        tile0 = a.tiles[min((int)blockIdx.x / (a.I / 64), a.max_tiles - 1)];
+        if (lane == 0) claim1 = atomicAdd(&sb->work_next, 1);   // raw counter value
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -266,41 +279,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     if (warp == 0) {
         // ------------------------------------------------------------ weight producer
         const uint64_t pol_w = ptx::policy_evict_first();
-        const int U1 = n_tiles * mb1;
-        const int total = U1 + n_tiles * (a.d / AROWS);
-        auto tile_of = [&](int u) { return u < U1 ? u / mb1 : (u - U1) / (a.d / AROWS); };
-        // unit u and its tile entry; the claim of the next unit (issued one unit
-        // earlier) and then the one after it stay in flight while a unit is issued
-        int u = __shfl_sync(0xffffffffu, claim0, 0);
-        int next_claim = claim1;   // lane 0
-        Tile tl = {0, 0, 0, 0}, tl_next = {0, 0, 0, 0};
-        if (u < total) tl = a.tiles[tile_of(u)];
         int ts = 0;   // stage sequence number
         bool ok = true;
         for (int i = 0; ok; ++i) {
             Unit U;
-            if (u < total) {
-                unit_coords(u, U1, a, U.down, U.tile, U.mb);
-                U.e = tl.e;
-                U.p0 = tl.p0;
-                U.n = tl.n;
-                U.stages = ((U.down ? a.I : a.d) + KS - 1) / KS;
-            } else {
-                U.down = -1;
-                U.tile = U.mb = U.e = U.p0 = U.n = U.stages = 0;
-            }
-            U.pad = 0;
-            const int u_next = u < total ? __shfl_sync(0xffffffffu, next_claim, 0) : total;
-            if (u_next < total) tl_next = a.tiles[tile_of(u_next)];
-            if (lane == 0) next_claim = u_next < total ? atomicAdd(&sb->work_next, 1) : total;
-            if (!ptx::mbar_wait_warp(&u_empty[i % UR], ((i / UR) & 1) ^ 1, abort_flag, WAIT_NS)) {
-                if (lane == 0) fail(8);
+            if (!take_unit(i, U)) {
+                if (lane == 0) fail(14);
                 break;
             }
-            if (lane == 0) {
-                uring[i % UR] = U;
-                ptx::mbar_arrive(&u_full[i % UR]);
-            }
+            if (lane == 0) *taken = i + 1;
             if (U.down < 0) break;
             const int K = U.down ? a.I : a.d;
             const int r0 = U.down ? U.e * a.d + U.mb * AROWS : U.mb * 64;
@@ -343,10 +330,64 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 __syncwarp();
             }
+        }
+        ptx::cp_async_wait_all();
+    } else if (warp == SCHED_WARP) {
+        // ------------------------------------------------------------ unit scheduler
+        const int U1 = n_tiles * mb1;
+        const int total = U1 + n_tiles * (a.d / AROWS);
+        auto tile_of = [&](int u) { return u < U1 ? u / mb1 : (u - U1) / (a.d / AROWS); };
+        // unit u and its tile entry; the claim of the next unit is in flight
+        // while this one waits for its turn.  A claim is kept as the raw counter
+        // value until it is used: arithmetic on it would wait for the atomic.
+        int u = (int)blockIdx.x;
+        int next_claim = claim1;   // lane 0
+        Tile tl = tile0, tl_next = {0, 0, 0, 0};
+        if (u >= U1 && u < total) tl = a.tiles[tile_of(u)];
+        for (int i = 0;; ++i) {
+            Unit U;
+            if (u < total) {
+                unit_coords(u, U1, a, U.down, U.tile, U.mb);
+                U.e = tl.e;
+                U.p0 = tl.p0;
+                U.n = tl.n;
+                U.stages = ((U.down ? a.I : a.d) + KS - 1) / KS;
+            } else {
+                U.down = -1;
+                U.tile = U.mb = U.e = U.p0 = U.n = U.stages = 0;
+            }
+            U.pad = 0;
+            const int u_next = u < total ? (int)gridDim.x + __shfl_sync(0xffffffffu, next_claim, 0) : total;
+            if (u_next < total) tl_next = a.tiles[tile_of(u_next)];
+            if (lane == 0) next_claim = u_next < total ? atomicAdd(&sb->work_next, 1) : total;
+            // publish unit i once the weight producer has taken unit i - LOOKAHEAD
+            // (bounded): claimed units wait in this CTA for a short while only
+            bool go = true;
+            if (lane == 0 && i >= LOOKAHEAD) {
+                const uint64_t t0 = ptx::globaltimer();
+                uint32_t it = 0;
+                while (*taken < i - LOOKAHEAD + 1) {
+                    __nanosleep(32);
+                    if ((++it & 63u) == 0u && (*abort_flag || ptx::globaltimer() - t0 > WAIT_NS)) {
+                        fail(15);
+                        go = false;
+                        break;
+                    }
+                }
+            }
+            if (!__shfl_sync(0xffffffffu, go ? 1 : 0, 0)) break;
+            if (!ptx::mbar_wait_warp(&u_empty[i % UR], ((i / UR) & 1) ^ 1, abort_flag, WAIT_NS)) {
+                if (lane == 0) fail(8);
+                break;
+            }
+            if (lane == 0) {
+                uring[i % UR] = U;
+                ptx::mbar_arrive(&u_full[i % UR]);
+            }
+            if (U.down < 0) break;
             u = u_next;
             tl = tl_next;
         }
-        ptx::cp_async_wait_all();
     } else if (warp == TOK_WARP) {
         // ------------------------------------------------------------ token producer
         const uint64_t pol_x = ptx::policy_evict_last();
@@ -398,7 +439,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 __syncwarp();
             }
         }
-    } else if (warp >= SF_WARP0) {
+    } else if (warp >= SF_WARP0 && warp < SF_WARP0 + 4) {
         // ------------------------------------------------------------ scale movers
         const int q = warp - SF_WARP0;    // TMEM lane quarter of this warp
         const int r = 32 * q + lane;      // weight row of this thread
@@ -463,12 +504,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (U.down < 0) break;
             bool ok = true;
             if (lane == 0) {
-                const int ab = i & 1;
+                const int ab = i % ACCB;
                 const uint32_t d_tmem = tmem + (ab * NMMA + m) * NB;
                 for (int c = 0; c < U.stages; ++c, ++ts) {
                     if ((c & 1) != m) continue;
                     const int s = ts % NSA, sbi = ts % NSB;
-                    if (c == m && !ptx::mbar_wait(&acc_empty[ab], ((i >> 1) & 1) ^ 1, abort_flag, WAIT_NS)) {
+                    if (c == m && !ptx::mbar_wait(&acc_empty[ab], ((i / ACCB) & 1) ^ 1, abort_flag, WAIT_NS)) {
                         fail(3);
                         ok = false;
                         break;
@@ -513,7 +554,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint32_t lane_base = (uint32_t)(32 * qd) << 16;
         const size_t tab_rows = (size_t)a.P + NT_MAX;
         for (int i = 0;; ++i) {
-            const int ab = i & 1;
+            const int ab = i % ACCB;
             // the four epilogue warps take one decision before their named
             // barriers: carry on, or leave together (they all read the same
             // ring entry, so they all see the end of the units together)
@@ -521,7 +562,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const bool got = take_unit(i, U);
             if (!got && lane == 0) fail(11);
             const bool end = got && U.down < 0;
-            if (!end && !*abort_flag && !ptx::mbar_wait_warp(&acc_full[ab], (i >> 1) & 1, abort_flag, WAIT_NS) &&
+            if (!end && !*abort_flag && !ptx::mbar_wait_warp(&acc_full[ab], (i / ACCB) & 1, abort_flag, WAIT_NS) &&
                 lane == 0)
                 fail(7);
             ptx::named_bar_sync(1, 128);
@@ -746,6 +787,7 @@ cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
     a.d = s.d;
     a.I = s.I;
     a.P = L.max_picks;
+    a.max_tiles = L.max_tiles;
     return launch_pdl(k_experts_mx<STMA, NTT>, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, tm_w13, tm_w2, tm_xq, tm_hq,
                       tm_w13s, tm_w2s, a);
 }

@@ -66,11 +66,14 @@ __device__ __forceinline__ void latch_status(StatusBlock* sb, int code, int deta
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  The block's kernels are launched so that the
 // next one may start while its predecessor is still running: every kernel
-// allows its successor to launch at once (pdl_trigger), does the set-up that
+// allows its successor to launch at once (pdl_trigger), does the work that
 // needs no predecessor's data, and calls pdl_wait, which returns when the
 // predecessor grid has completed and its writes are visible, before it reads
-// or writes anything the stream's earlier kernels touch.  Without the launch
-// attribute (or after a non-kernel stream operation) pdl_wait returns at once.
+// or writes anything the stream's earlier kernels touch.  Before the wait a
+// kernel reads only the caller's weights and bias, which none of the block's
+// kernels writes; a kernel of the caller's that precedes the block triggers
+// its successor only at exit, so the block never starts ahead of it.  Without
+// the launch attribute pdl_wait returns at once.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }

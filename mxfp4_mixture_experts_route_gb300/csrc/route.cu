@@ -104,11 +104,92 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
         // thread i: token i / 8, expert i % 8 of the tile
         const int t = threadIdx.x / RT_EXPERTS, ee = threadIdx.x % RT_EXPERTS;
         const int eg = blockIdx.x * RT_EXPERTS + ee;
+        float pz[RT_MAX_CLUSTER];
+#pragma unroll
+        for (int r = 0; r < RT_MAX_CLUSTER; ++r)   // the remote loads, all in flight together
+            pz[r] = r < kslices ? cluster.map_shared_rank(part, r)[t * RT_EXPERTS + ee] : 0.f;
         float z = 0.f;
-        for (int r = 0; r < kslices; ++r) z += cluster.map_shared_rank(part, r)[t * RT_EXPERTS + ee];
+#pragma unroll
+        for (int r = 0; r < RT_MAX_CLUSTER; ++r) z += pz[r];   // K-range order
         if (t < nt && eg < E) L[(size_t)(t0 + t) * E + eg] = off ? z + off[eg] : z;
     }
     cluster.sync();   // every CTA keeps its shared memory until the first has read it
+}
+
+// The same logits for a few tokens (S <= NTOK) and at most NR 256-K rounds per
+// CTA: a lane issues every load of its weight slice (before the wait on the
+// previous kernel) and of the token rows at once, straight from global memory
+// (the rows are shared by all CTAs through L2), with no shared-memory staging.
+template <int NTOK, int NR>
+__global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* __restrict__ x,
+                                                           const __nv_bfloat16* __restrict__ wg,
+                                                           const float* __restrict__ off, float* __restrict__ L,
+                                                           int S, int d, int E, int kslices) {
+    __shared__ float part[NTOK * RT_EXPERTS];
+    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    const int e = blockIdx.x * RT_EXPERTS + warp, ks = blockIdx.y;
+    const int nk = d / 128;
+    const int k_begin = (int)((long long)nk * ks / kslices) * 128;
+    const int k_end = (int)((long long)nk * (ks + 1) / kslices) * 128;
+    pdl_trigger();
+    uint4 w[NR];
+    int q16[NR];
+#pragma unroll
+    for (int r = 0; r < NR; ++r) {
+        const int kc = k_begin + RT_KC * r;
+        q16[r] = kc < k_end ? min(RT_KC, k_end - kc) / 8 : 0;
+        w[r] = make_uint4(0, 0, 0, 0);
+        if (e < E && lane < q16[r]) w[r] = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)e * d + kc) + lane);
+    }
+    pdl_wait();   // x may come from the stream's previous kernel
+    uint4 xv[NR][NTOK];
+#pragma unroll
+    for (int r = 0; r < NR; ++r)
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) {
+            xv[r][t] = make_uint4(0, 0, 0, 0);
+            if (t < S && lane < q16[r])
+                xv[r][t] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)t * d + k_begin + RT_KC * r) + lane);
+        }
+    float acc[NTOK];
+#pragma unroll
+    for (int t = 0; t < NTOK; ++t) {
+        float a = 0.f;
+#pragma unroll
+        for (int r = 0; r < NR; ++r) {
+            const uint4 v = xv[r][t], ww = w[r];
+            a = fmaf(bf_lo(v.x), bf_lo(ww.x), a);
+            a = fmaf(bf_hi(v.x), bf_hi(ww.x), a);
+            a = fmaf(bf_lo(v.y), bf_lo(ww.y), a);
+            a = fmaf(bf_hi(v.y), bf_hi(ww.y), a);
+            a = fmaf(bf_lo(v.z), bf_lo(ww.z), a);
+            a = fmaf(bf_hi(v.z), bf_hi(ww.z), a);
+            a = fmaf(bf_lo(v.w), bf_lo(ww.w), a);
+            a = fmaf(bf_hi(v.w), bf_hi(ww.w), a);
+        }
+#pragma unroll
+        for (int m = 16; m >= 1; m >>= 1) a += __shfl_xor_sync(0xffffffffu, a, m);
+        acc[t] = a;
+    }
+    if (lane == 0) {
+#pragma unroll
+        for (int t = 0; t < NTOK; ++t) part[t * RT_EXPERTS + warp] = acc[t];
+    }
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    if (ks == 0 && threadIdx.x < NTOK * RT_EXPERTS) {
+        const int t = threadIdx.x / RT_EXPERTS, ee = threadIdx.x % RT_EXPERTS;
+        const int eg = blockIdx.x * RT_EXPERTS + ee;
+        float pz[RT_MAX_CLUSTER];
+#pragma unroll
+        for (int r = 0; r < RT_MAX_CLUSTER; ++r)
+            pz[r] = r < kslices ? cluster.map_shared_rank(part, r)[t * RT_EXPERTS + ee] : 0.f;
+        float z = 0.f;
+#pragma unroll
+        for (int r = 0; r < RT_MAX_CLUSTER; ++r) z += pz[r];
+        if (t < S && eg < E) L[(size_t)t * E + eg] = off ? z + off[eg] : z;
+    }
+    cluster.sync();
 }
 
 // One warp per token (see topk_token).
@@ -117,13 +198,18 @@ __global__ void __launch_bounds__(256) k_topk(const float* __restrict__ L, const
                                               float* __restrict__ wout) {
     const int lane = threadIdx.x & 31;
     pdl_trigger();
-    pdl_wait();
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (t >= S) return;
-    if (E <= 256)
-        topk_token<256 / 32>(L + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
-    else
-        topk_token<512 / 32>(L + (size_t)t * E, bias, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
+    if (E <= 256) {
+        float b[256 / 32];
+        load_bias(bias, E, lane, b);   // an input of the call: read before the wait
+        pdl_wait();
+        if (t < S) topk_token(L + (size_t)t * E, b, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
+    } else {
+        float b[512 / 32];
+        load_bias(bias, E, lane, b);
+        pdl_wait();
+        if (t < S) topk_token(L + (size_t)t * E, b, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
+    }
 }
 
 }  // namespace
@@ -155,8 +241,14 @@ cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Pt
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
+    // few tokens and at most two 256-K rounds per CTA: the variant without staging
+    const int nk = s.d / 128;
+    const bool few = s.S <= 8 && (nk + ks - 1) / ks <= 2 * (RT_KC / 128);
+    if (few) cfg.gridDim = dim3((s.E + RT_EXPERTS - 1) / RT_EXPERTS, ks, 1);
     timing_begin(K_ROUTER, st);
-    cudaError_t e = cudaLaunchKernelEx(&cfg, k_router, p.x, p.w_gate, p.logit_off, logits, s.S, s.d, s.E, ks);
+    cudaError_t e = few ? cudaLaunchKernelEx(&cfg, k_router_few<8, 2>, p.x, p.w_gate, p.logit_off, logits, s.S, s.d,
+                                             s.E, ks)
+                        : cudaLaunchKernelEx(&cfg, k_router, p.x, p.w_gate, p.logit_off, logits, s.S, s.d, s.E, ks);
     timing_end(st);
     return e;
 }

@@ -188,11 +188,13 @@ __global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* __restr
                                                             float* __restrict__ weights, SortOut o) {
     extern __shared__ int32_t smem[];
     pdl_trigger();
-    pdl_wait();
     int32_t* sids = smem + sort_smem_ints(E);   // [S][k]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    float b[MAXE];
+    load_bias(bias, E, lane, b);   // an input of the call: read before the wait
+    pdl_wait();
     for (int t = warp; t < S; t += SORT_THREADS / 32)
-        topk_token<MAXE>(L + (size_t)t * E, bias, E, k, lane, sids + (size_t)t * k, weights + (size_t)t * k);
+        topk_token(L + (size_t)t * E, b, E, k, lane, sids + (size_t)t * k, weights + (size_t)t * k);
     __syncthreads();
     for (int i = threadIdx.x; i < S * k; i += SORT_THREADS) ids[i] = sids[i];
     sort_picks(sids, S, E, k, o, smem);

@@ -43,20 +43,30 @@ __device__ __forceinline__ void lane_best(const uint32_t (&key)[MAXE], uint32_t&
     bi = ii[0];
 }
 
-// Lane l holds experts l, l + 32, ... (E <= 32 * MAXE).  Each round takes the
-// warp's largest key (one redux), the lowest expert id among the lanes that
-// hold it (a second redux), and lets the owning lane retire it and find its
-// next best.  Writes ids_out[0..k) in ascending id and w_out[0..k).
+// The lane's slots of the bias (lane l holds experts l, l + 32, ...).
 template <int MAXE>
-__device__ __forceinline__ void topk_token(const float* __restrict__ Lrow, const float* __restrict__ bias, int E,
-                                           int k, int lane, int32_t* ids_out, float* w_out) {
-    float s[MAXE], z[MAXE], b[MAXE];
+__device__ __forceinline__ void load_bias(const float* __restrict__ bias, int E, int lane, float (&b)[MAXE]) {
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) {
+        const int e = lane + 32 * i;
+        b[i] = e < E ? bias[e] : 0.f;
+    }
+}
+
+// Lane l holds experts l, l + 32, ... (E <= 32 * MAXE), b from load_bias.
+// Each round takes the warp's largest key (one redux), the lowest expert id
+// among the lanes that hold it (a second redux), and lets the owning lane
+// retire it and find its next best.  Writes ids_out[0..k) in ascending id and
+// w_out[0..k).
+template <int MAXE>
+__device__ __forceinline__ void topk_token(const float* __restrict__ Lrow, const float (&b)[MAXE], int E, int k,
+                                           int lane, int32_t* ids_out, float* w_out) {
+    float s[MAXE], z[MAXE];
     uint32_t key[MAXE];
 #pragma unroll
     for (int i = 0; i < MAXE; ++i) {           // independent loads, all in flight together
         const int e = lane + 32 * i;
         z[i] = e < E ? Lrow[e] : 0.f;
-        b[i] = e < E ? bias[e] : 0.f;
     }
 #pragma unroll
     for (int i = 0; i < MAXE; ++i) {
