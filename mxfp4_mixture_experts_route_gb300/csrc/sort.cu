@@ -10,6 +10,7 @@
 #include "moe_internal.cuh"
 #include "tc_ptx.cuh"
 #include "topk.cuh"
+#include "quant.cuh"
 
 #include <algorithm>
 
@@ -200,17 +201,8 @@ __global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* __restr
     sort_picks(sids, S, E, k, o, smem);
 }
 
-// Token rows of the expert GEMMs.  For every valid pick p < n_picks, token
-// t = src[p] / k: rows 2p and 2p + 1 of xq hold hi = e4m3(x[t] / 2^s) and
-// lo = e4m3(x[t] / 2^s - hi) for every 32-element block, and the scale table
-// xs holds the block's e8m0 byte s + 127, chosen so that the block's largest
-// magnitude divided by 2^s lies in [128, 256) (clamped to bytes 1..247).  For
-// a bf16 x the two rows add up to x / 2^s exactly, but for elements more than
-// 2^9 below the block maximum (there the error is below 2^-17 of it).  The
-// unused bytes of the last stage's scale rows of xs and hs (K / 32 not a
-// multiple of 8) are set to 127 (scale 1), as their codes are zero.
-// grid (max_picks), blockDim = d / 8 rounded up to a warp (at most 1024): a
-// thread takes 8 elements, four threads a block, in one pass for d <= 8192.
+// Token rows of the expert GEMMs (see quantize_pick).  grid (max_picks),
+// blockDim = d / 8 rounded up to a warp (at most 1024), one pick a CTA.
 __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __restrict__ x,
                                                       const int32_t* __restrict__ src, int k, int d, int I, int P,
                                                       uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
@@ -221,56 +213,7 @@ __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __re
     const int p = blockIdx.x;
     const int sp = src[p];                 // read beside n_picks: src has max_picks entries
     if (p >= sb->n_picks) return;
-    const int t = sp / k;
-    const size_t rows = (size_t)P + NT_MAX;
-    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    uint8_t* hi_row = xq + (size_t)(2 * p) * d;
-    uint8_t* lo_row = hi_row + d;
-    for (int c0 = 0; c0 < d / 8; c0 += blockDim.x) {
-        const int c = c0 + threadIdx.x;
-        const bool act = c < d / 8;        // whole blocks of four threads (d / 8 is a multiple of 16)
-        const uint4 v = act ? __ldg(in + c) : make_uint4(0, 0, 0, 0);
-        const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
-        float f[8];
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            f[2 * j] = __uint_as_float(wv[j] << 16);
-            f[2 * j + 1] = __uint_as_float(wv[j] & 0xFFFF0000u);
-        }
-        uint32_t amax = 0;
-#pragma unroll
-        for (int j = 0; j < 8; ++j) amax = max(amax, __float_as_uint(fabsf(f[j])));
-        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 1));
-        amax = max(amax, __shfl_xor_sync(0xffffffffu, amax, 2));
-        int e = (int)((amax >> 23) & 0xFFu) - 7;
-        e = e < 1 ? 1 : (e > 247 ? 247 : e);
-        const float mult = __uint_as_float((uint32_t)(254 - e) << 23);   // 2^-(e - 127)
-        uint32_t hw[2] = {0, 0}, lw[2] = {0, 0};
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-            const float a0 = f[2 * j] * mult, a1 = f[2 * j + 1] * mult;
-            const uint32_t h2 = ptx::cvt_e4m3x2(a0, a1);
-            float b0, b1;
-            ptx::e4m3x2_to_f32(h2, b0, b1);
-            const uint32_t l2 = ptx::cvt_e4m3x2(a0 - b0, a1 - b1);
-            hw[j >> 1] |= h2 << (16 * (j & 1));
-            lw[j >> 1] |= l2 << (16 * (j & 1));
-        }
-        if (act) {
-            *reinterpret_cast<uint2*>(hi_row + 8 * c) = make_uint2(hw[0], hw[1]);
-            *reinterpret_cast<uint2*>(lo_row + 8 * c) = make_uint2(lw[0], lw[1]);
-            if ((c & 3) == 0) {
-                const int blk = c >> 2;
-                xs[((size_t)(blk >> 3) * rows + p) * TOKEN_SCALE_ROW + (blk & 7)] = (uint8_t)e;
-            }
-        }
-    }
-    if (threadIdx.x < 8) {
-        const int j = threadIdx.x;
-        const int nbx = d / 32, nbh = I / 32;
-        if ((nbx & 7) && j >= (nbx & 7)) xs[((size_t)(nbx >> 3) * rows + p) * TOKEN_SCALE_ROW + j] = 127;
-        if ((nbh & 7) && j >= (nbh & 7)) hs[((size_t)(nbh >> 3) * rows + p) * TOKEN_SCALE_ROW + j] = 127;
-    }
+    quantize_pick(x, sp / k, p, d, I, (size_t)P + NT_MAX, xq, xs, hs, threadIdx.x, blockDim.x);
 }
 
 }  // namespace
