@@ -77,8 +77,9 @@ constexpr int TMEM_COLS = 512;
 constexpr int NMMA = 2;                      // MMA-issuing warps (one thread each)
 // One stage's scale slot in TMEM, 64 columns: the weight scales of K steps
 // 0-3 at +0 and of K steps 4-7 at +16 (row m of the tile in lane m, column
-// + m / 32), the token scales at +32 and +48 (column n in lane n of every lane
-// quarter).  Every scale address the MMA gets is a multiple of 16 columns.
+// + m / 32), the token scales at +32 and +48 (column n in lane n mod 32 of
+// every lane quarter, column + n / 32).  Every scale address the MMA gets is a
+// multiple of 16 columns.
 constexpr int SF_SLOT = 64;
 constexpr int SF_A1 = 16, SF_B0 = 32, SF_B1 = 48;
 constexpr int MMA_WARP0 = 1, EPI_WARP0 = 3, TOK_WARP = 7, SF_WARP0 = 8, SCHED_WARP = 12;
@@ -102,6 +103,7 @@ struct Cfg {
     // buffers when they fit beside six scale slots, so that short units do not
     // wait for the epilogue to drain the buffer of two units back
     static constexpr int ACCB = NTT == 8 ? 4 : 2;
+    static constexpr int BSG = (NB + 31) / 32;                 // TMEM columns of one group of token scales
     static constexpr int SF_COL0 = ACCB * NMMA * NB;           // TMEM columns of the scale slots
 
     static constexpr int SC_ROW = STMA ? 16 : 8;               // e8m0 bytes of a row in a stage
@@ -463,10 +465,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 const uint8_t* st = wst + s * C::A_STAGE;
                 const uint2 wa = *reinterpret_cast<const uint2*>(st + C::SC_OFF + C::SC_ROW * r + (STMA ? 8 * (c & 1) : 0));
-                // token column n = lane: pick lane / 2 (hi and lo row); lanes past the
-                // tile's 2 NTT columns are never read
-                const uint2 wb = *reinterpret_cast<const uint2*>(
-                    tsc + sbi * BS_BYTES + TOKEN_SCALE_ROW * ((lane >> 1) & (NTT - 1)));
+                // token column n = 32 g + lane (g < BSG): pick n / 2 (its hi and lo
+                // row); columns past the tile's 2 NTT are never read
+                uint32_t bx[C::BSG], by[C::BSG];
+#pragma unroll
+                for (int g = 0; g < C::BSG; ++g) {
+                    const uint2 wb = *reinterpret_cast<const uint2*>(
+                        tsc + sbi * BS_BYTES + TOKEN_SCALE_ROW * ((16 * g + (lane >> 1)) & (NTT - 1)));
+                    bx[g] = wb.x;
+                    by[g] = wb.y;
+                }
                 // 0xFF is NaN in e8m0
                 const uint32_t nan_a = __vcmpeq4(wa.x, 0xFFFFFFFFu) | __vcmpeq4(wa.y, 0xFFFFFFFFu);
                 if (nan_a) latch_status(sb, MOE_ERR_BAD_SCALE, 255);
@@ -477,9 +485,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 // columns of these lanes are never read
                 ptx::tmem_st4_rep(tmem + lane_base + col, wa.x);
                 ptx::tmem_st4_rep(tmem + lane_base + col + SF_A1, wa.y);
-                // token column n = lane (pick lane / 2, hi or lo row), in every lane quarter
-                ptx::tmem_st4_rep(tmem + lane_base + col + SF_B0, wb.x);
-                ptx::tmem_st4_rep(tmem + lane_base + col + SF_B1, wb.y);
+                // token column n: lane n mod 32 of every lane quarter, column + n / 32
+                if constexpr (C::BSG == 1) {
+                    ptx::tmem_st4_rep(tmem + lane_base + col + SF_B0, bx[0]);
+                    ptx::tmem_st4_rep(tmem + lane_base + col + SF_B1, by[0]);
+                } else {
+                    static_assert(C::BSG == 2, "token scale groups of one or two columns");
+                    ptx::tmem_st2(tmem + lane_base + col + SF_B0, bx[0], bx[1]);
+                    ptx::tmem_st2(tmem + lane_base + col + SF_B1, by[0], by[1]);
+                }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
@@ -800,8 +814,10 @@ cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p,
     cudaError_t e;
     if (L.nt == 8)
         e = stma ? launch_mx<true, 8>(s, L, p, st) : launch_mx<false, 8>(s, L, p, st);
-    else
+    else if (L.nt == 16)
         e = stma ? launch_mx<true, 16>(s, L, p, st) : launch_mx<false, 16>(s, L, p, st);
+    else
+        e = stma ? launch_mx<true, 32>(s, L, p, st) : launch_mx<false, 32>(s, L, p, st);
     timing_end(st);
     return e;
 }

@@ -11,9 +11,15 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Picks per expert tile: 8 while the average expert gets at most 2 picks (the
 // tile then carries little padding, and the expert kernel's smaller token
-// stages leave room for one more weight stage), else 16 (with more picks per
-// expert a second tile, which reads the expert's weights again, gets likely).
-int tile_picks(const moe_shape& s) { return (int64_t)s.S * s.k <= 2 * (int64_t)s.E ? 8 : 16; }
+// stages leave room for one more weight stage); 32 once it gets 32 or more
+// (fewer, wider MMAs per weight byte where the expert GEMMs turn compute
+// bound); else 16 (with more picks per expert a second tile, which reads the
+// expert's weights again, gets likely).
+int tile_picks(const moe_shape& s) {
+    const int64_t picks = (int64_t)s.S * s.k;
+    if (picks <= 2 * (int64_t)s.E) return 8;
+    return picks >= 32 * (int64_t)s.E ? 32 : 16;
+}
 
 WsLayout ws_layout(const moe_shape& s) {
     WsLayout L{};

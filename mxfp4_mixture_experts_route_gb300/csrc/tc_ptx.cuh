@@ -323,6 +323,11 @@ __host__ __device__ constexpr uint32_t idesc_mx_e2m1_e4m3(int m, int n, int asf,
            ((uint32_t)(m >> 4) << 24) | ((uint32_t)asf << 29);
 }
 
+// 32 lanes x 2 consecutive 32-bit TMEM columns (taddr's column a multiple of 2)
+__device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t v0, uint32_t v1) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v0), "r"(v1) : "memory");
+}
+
 // 32 lanes x 4 consecutive 32-bit TMEM columns, all four set to v (taddr's
 // column a multiple of 4)
 __device__ __forceinline__ void tmem_st4_rep(uint32_t taddr, uint32_t v) {
