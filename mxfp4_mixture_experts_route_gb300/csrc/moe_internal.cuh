@@ -1,6 +1,7 @@
 // Internal declarations shared by the translation units of libmoe.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <cuda_bf16.h>
 #include <stddef.h>
@@ -58,6 +59,13 @@ struct WsLayout {
 };
 
 WsLayout ws_layout(const moe_shape& s);
+
+// Host helpers of the tensor-core kernels (experts_mx.cu): a rank-r tiled
+// tensor map (dims[0] innermost; strides[i] = byte stride of dims[i+1]) and
+// the device's SM count.
+bool make_map(CUtensorMap* m, CUtensorMapDataType dt, const void* base, int rank, const uint64_t* dims,
+              const uint64_t* strides, const uint32_t* box, CUtensorMapSwizzle sw);
+int num_sms();
 int router_kslices(const moe_shape& s, int num_sms);
 
 __device__ __forceinline__ void latch_status(StatusBlock* sb, int code, int detail) {
@@ -124,6 +132,9 @@ struct Ptrs {
 };
 
 cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+// the router's tensor-core kernel (S >= 64, E a multiple of 128)
+bool router_tc_fits(const moe_shape& s);
+cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 // moe_forward at small S: top-k and sort in one kernel (needs the logits)
 bool topk_sort_fits(const moe_shape& s);

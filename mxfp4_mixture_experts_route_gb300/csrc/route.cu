@@ -225,6 +225,12 @@ int router_kslices(const moe_shape& s, int num_sms) {
 }
 
 cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    if (router_tc_fits(s)) {
+        timing_begin(K_ROUTER, st);
+        const cudaError_t e = launch_router_tc(s, L, p, st);
+        timing_end(st);
+        return e;
+    }
     float* logits = reinterpret_cast<float*>(p.ws + L.logits);
     const int ks = L.router_kslices;
     cudaLaunchConfig_t cfg = {};
