@@ -72,9 +72,12 @@ constexpr int A_TX = AROWS * KS / 2;         // packed bytes of a weight tile: t
 #ifndef MOE_MX_TOKEN_STAGES
 #define MOE_MX_TOKEN_STAGES 4
 #endif
-constexpr int NSB = MOE_MX_TOKEN_STAGES;     // token-tile stages
+#ifndef MOE_MX_WIDE_TOKEN_STAGES
+#define MOE_MX_WIDE_TOKEN_STAGES 2
+#endif
+constexpr int NSB_DEF = MOE_MX_TOKEN_STAGES; // token-tile stages (two for 64-pick tiles)
 constexpr int TMEM_COLS = 512;
-constexpr int NMMA = 2;                      // MMA-issuing warps (one thread each)
+constexpr int NMMA_MAX = 2;                  // MMA-issuing warps (one thread each; one for 64-pick tiles)
 // One stage's scale slot in TMEM, 64 columns: the weight scales of K steps
 // 0-3 at +0 and of K steps 4-7 at +16 (row m of the tile in lane m, column
 // + m / 32), the token scales at +32 and +48 (column n in lane n mod 32 of
@@ -96,6 +99,9 @@ constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 template <bool STMA, int NTT>
 struct Cfg {
     static constexpr int NB = 2 * NTT;                         // MMA N: a hi and a lo row per pick
+    static constexpr int NMMA = NTT >= 64 ? 1 : NMMA_MAX;      // issuers (TMEM: one N = 128 accumulator each)
+    static constexpr int NSB = NTT >= 64 ? MOE_MX_WIDE_TOKEN_STAGES : NSB_DEF;   // token stages (32 KB at 64 picks)
+    static constexpr int EC = NTT < 16 ? NTT : 16;             // picks per epilogue chunk
     static constexpr int B_SLAB = NB * 128;                    // one 128-K slab of the token tile
     static constexpr int B_SMEM = 2 * B_SLAB;                  // a token stage (4 or 8 KB)
     static constexpr int BS_BYTES = NTT * TOKEN_SCALE_ROW;     // the tile's token scale rows
@@ -104,6 +110,7 @@ struct Cfg {
     // wait for the epilogue to drain the buffer of two units back
     static constexpr int ACCB = NTT == 8 ? 4 : 2;
     static constexpr int BSG = (NB + 31) / 32;                 // TMEM columns of one group of token scales
+    static_assert(NTT <= NT_MAX, "token tables are padded by NT_MAX rows");
     static constexpr int SF_COL0 = ACCB * NMMA * NB;           // TMEM columns of the scale slots
 
     static constexpr int SC_ROW = STMA ? 16 : 8;               // e8m0 bytes of a row in a stage
@@ -111,7 +118,7 @@ struct Cfg {
     static constexpr int SC_OFF = A_SMEM;                      // within a weight stage
     static constexpr int A_STAGE = (A_SMEM + SC_BYTES + 1023) / 1024 * 1024;
     static constexpr int B_STAGE = B_SMEM;                     // the token scale rows sit apart
-    static constexpr int XCH_STRIDE = NTT + 1;
+    static constexpr int XCH_STRIDE = EC + 1;
     static constexpr int XCH_BYTES = 64 * XCH_STRIDE * 4;
     static constexpr int RING_BYTES = UR * 32;
     static constexpr int TSC_BYTES = NSB * BS_BYTES;
@@ -180,7 +187,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                  const Args a) {
     using C = Cfg<STMA, NTT>;
     constexpr int NSA = C::NSA, NB = C::NB, B_SLAB = C::B_SLAB, B_SMEM = C::B_SMEM, BS_BYTES = C::BS_BYTES;
-    constexpr int SF_COL0 = C::SF_COL0, ACCB = C::ACCB;
+    constexpr int SF_COL0 = C::SF_COL0, ACCB = C::ACCB, NSB = C::NSB, NMMA = C::NMMA, EC = C::EC;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* wst = smem;                                  // weight stages [NSA][A_STAGE]
@@ -198,8 +205,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* acc_empty = acc_full + ACCB;  // [ACCB]
     uint64_t* u_full = acc_empty + ACCB;    // [UR]
     uint64_t* u_empty = u_full + UR;        // [UR]
-    uint64_t* fin = u_empty + UR;           // [NMMA]
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + NMMA);
+    uint64_t* fin = u_empty + UR;           // [NMMA_MAX]
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + NMMA_MAX);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
     volatile int* epi_flag = abort_flag + 1;
     volatile int* taken = abort_flag + 2;   // units the weight producer has taken
@@ -489,10 +496,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if constexpr (C::BSG == 1) {
                     ptx::tmem_st4_rep(tmem + lane_base + col + SF_B0, bx[0]);
                     ptx::tmem_st4_rep(tmem + lane_base + col + SF_B1, by[0]);
-                } else {
-                    static_assert(C::BSG == 2, "token scale groups of one or two columns");
+                } else if constexpr (C::BSG == 2) {
                     ptx::tmem_st2(tmem + lane_base + col + SF_B0, bx[0], bx[1]);
                     ptx::tmem_st2(tmem + lane_base + col + SF_B1, by[0], by[1]);
+                } else {
+                    static_assert(C::BSG == 4, "token scale groups of one, two or four columns");
+                    ptx::tmem_st4(tmem + lane_base + col + SF_B0, bx[0], bx[1], bx[2], bx[3]);
+                    ptx::tmem_st4(tmem + lane_base + col + SF_B1, by[0], by[1], by[2], by[3]);
                 }
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
@@ -502,8 +512,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         }
     } else if (warp >= MMA_WARP0 && warp < MMA_WARP0 + NMMA) {
         // ------------------------------------------------------------ MMA issuers
-        // Issuer m takes the stages c of every unit with c mod 2 == m (all
-        // eight K steps of each), so the two issue loops overlap on different
+        // Issuer m takes the stages c of every unit with c mod NMMA == m (all
+        // eight K steps of each), so two issue loops overlap on different
         // stages.  It waits only on sf_full: the scale movers arrive there
         // after they have waited on the stage's weight and token barriers, so
         // both TMA copies are complete and visible once sf_full completes.
@@ -521,7 +531,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 const int ab = i % ACCB;
                 const uint32_t d_tmem = tmem + (ab * NMMA + m) * NB;
                 for (int c = 0; c < U.stages; ++c, ++ts) {
-                    if ((c & 1) != m) continue;
+                    if (c % NMMA != m) continue;
                     const int s = ts % NSA, sbi = ts % NSB;
                     if (c == m && !ptx::mbar_wait(&acc_empty[ab], ((i / ACCB) & 1) ^ 1, abort_flag, WAIT_NS)) {
                         fail(3);
@@ -561,6 +571,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::mbar_wait(&fin[m], 0, abort_flag, WAIT_NS);
         }
         __syncwarp();
+    } else if (warp >= MMA_WARP0 && warp < MMA_WARP0 + NMMA_MAX) {
+        // an issuer warp with nothing to do: the widest tiles have a single issuer
     } else {
         // ------------------------------------------------------------ epilogue
         const int qd = warp & 3;
@@ -584,116 +596,127 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             ptx::named_bar_sync(1, 128);
             if (*epi_flag || end) break;
             ptx::tc_fence_after();
-            // v[n]: the issuers' stages, hi + lo column of pick n
-            float v[NTT];
-#pragma unroll
-            for (int n = 0; n < NTT; ++n) v[n] = 0.f;
             const int n_iss = U.stages < NMMA ? U.stages : NMMA;   // issuers that had a stage
+            const int ii = U.mb * 64 + r;        // gate_up: h row of lanes 0..63
+            const int blk = ii / 32;             // its 32-row block of h
+            // the tile's picks in chunks of EC: v[n] = the issuers' stages, hi + lo
+            // column of pick ch + n
+#pragma unroll 1
+            for (int ch = 0; ch < NTT; ch += EC) {
+                float v[EC];
 #pragma unroll
-            for (int mm = 0; mm < NMMA; ++mm) {
-                if (mm >= n_iss) break;
-                uint32_t t[NB];
+                for (int n = 0; n < EC; ++n) v[n] = 0.f;
 #pragma unroll
-                for (int j = 0; j < NB / 16; ++j)
-                    ptx::tmem_ld16(tmem + lane_base + (ab * NMMA + mm) * NB + 16 * j, t + 16 * j);
-                ptx::tmem_ld_wait();
+                for (int mm = 0; mm < NMMA; ++mm) {
+                    if (mm >= n_iss) break;
+                    uint32_t t[2 * EC];
 #pragma unroll
-                for (int n = 0; n < NTT; ++n) v[n] += __uint_as_float(t[2 * n]) + __uint_as_float(t[2 * n + 1]);
-            }
-            ptx::tc_fence_before();
-            __syncwarp();
-            if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);
-            if (!U.down) {
-                // lanes 0..63: gate of rows mb*64 + r; lanes 64..127: up of the same rows
-                if (r >= 64) {
+                    for (int j = 0; j < 2 * EC / 16; ++j)
+                        ptx::tmem_ld16(tmem + lane_base + (ab * NMMA + mm) * NB + 2 * ch + 16 * j, t + 16 * j);
+                    ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int n = 0; n < NTT; ++n) xch[(r - 64) * C::XCH_STRIDE + n] = v[n];
+                    for (int n = 0; n < EC; ++n) v[n] += __uint_as_float(t[2 * n]) + __uint_as_float(t[2 * n + 1]);
                 }
-                ptx::named_bar_sync(1, 128);
-                if (r < 64) {
-                    // warp qd (0 or 1) holds the 32 rows of h block mb*2 + qd
-                    const int ii = U.mb * 64 + r;
-                    const int blk = ii / 32;
-                    float h[NTT];
+                if (ch + EC >= NTT) {   // the accumulator is read out
+                    ptx::tc_fence_before();
+                    __syncwarp();
+                    if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);
+                }
+                if (!U.down) {
+                    // lanes 0..63: gate of rows mb*64 + r; lanes 64..127: up of the same rows
+                    if (r >= 64) {
 #pragma unroll
-                    for (int n = 0; n < NTT; ++n) {
-                        const float gv = v[n];
-                        const float uv = xch[r * C::XCH_STRIDE + n];
-                        h[n] = n < U.n ? gv / (1.0f + __expf(-gv)) * uv : 0.f;
+                        for (int n = 0; n < EC; ++n) xch[(r - 64) * C::XCH_STRIDE + n] = v[n];
                     }
+                    ptx::named_bar_sync(1, 128);
+                    if (r < 64) {
+                        // warp qd (0 or 1) holds the 32 rows of h block mb*2 + qd
+                        float h[EC];
 #pragma unroll
-                    for (int n = 0; n < NTT; n += 2) {
-                        uint32_t byte2[2];
-                        float hs2[2];
-#pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[n + z])));
-                            int e = (int)((amax >> 23) & 0xFFu) - 7;
-                            e = e < 1 ? 1 : (e > 247 ? 247 : e);
-                            byte2[z] = (uint32_t)e;
-                            hs2[z] = h[n + z] * __uint_as_float((uint32_t)(254 - e) << 23);   // h / 2^(e - 127)
+                        for (int n = 0; n < EC; ++n) {
+                            const float gv = v[n];
+                            const float uv = xch[r * C::XCH_STRIDE + n];
+                            h[n] = ch + n < U.n ? gv / (1.0f + __expf(-gv)) * uv : 0.f;
                         }
-                        const uint32_t hi2 = ptx::cvt_e4m3x2(hs2[0], hs2[1]);
-                        float f0, f1;
-                        ptx::e4m3x2_to_f32(hi2, f0, f1);
-                        const uint32_t lo2 = ptx::cvt_e4m3x2(hs2[0] - f0, hs2[1] - f1);
 #pragma unroll
-                        for (int z = 0; z < 2; ++z) {
-                            if (n + z < U.n) {
-                                const size_t p = (size_t)(U.p0 + n + z);
-                                a.hq[(2 * p) * a.I + ii] = (uint8_t)(hi2 >> (8 * z));
-                                a.hq[(2 * p + 1) * a.I + ii] = (uint8_t)(lo2 >> (8 * z));
-                                if (lane == 0)
-                                    a.hs[((size_t)(blk >> 3) * tab_rows + p) * TOKEN_SCALE_ROW + (blk & 7)] =
-                                        (uint8_t)byte2[z];
+                        for (int n = 0; n < EC; n += 2) {
+                            uint32_t byte2[2];
+                            float hs2[2];
+#pragma unroll
+                            for (int z = 0; z < 2; ++z) {
+                                const uint32_t amax = __reduce_max_sync(0xffffffffu, __float_as_uint(fabsf(h[n + z])));
+                                int e = (int)((amax >> 23) & 0xFFu) - 7;
+                                e = e < 1 ? 1 : (e > 247 ? 247 : e);
+                                byte2[z] = (uint32_t)e;
+                                hs2[z] = h[n + z] * __uint_as_float((uint32_t)(254 - e) << 23);   // h / 2^(e - 127)
+                            }
+                            const uint32_t hi2 = ptx::cvt_e4m3x2(hs2[0], hs2[1]);
+                            float f0, f1;
+                            ptx::e4m3x2_to_f32(hi2, f0, f1);
+                            const uint32_t lo2 = ptx::cvt_e4m3x2(hs2[0] - f0, hs2[1] - f1);
+#pragma unroll
+                            for (int z = 0; z < 2; ++z) {
+                                if (ch + n + z < U.n) {
+                                    const size_t p = (size_t)(U.p0 + ch + n + z);
+                                    a.hq[(2 * p) * a.I + ii] = (uint8_t)(hi2 >> (8 * z));
+                                    a.hq[(2 * p + 1) * a.I + ii] = (uint8_t)(lo2 >> (8 * z));
+                                    if (lane == 0)
+                                        a.hs[((size_t)(blk >> 3) * tab_rows + p) * TOKEN_SCALE_ROW + (blk & 7)] =
+                                            (uint8_t)byte2[z];
+                                }
                             }
                         }
                     }
-                    ptx::fence_proxy_async_global();
+                    ptx::named_bar_sync(1, 128);   // xch is written again by the next chunk
+                } else {
+                    const int m = U.mb * AROWS + r;
+#pragma unroll
+                    for (int n = 0; n < EC; ++n)
+                        if (ch + n < U.n) a.y[(size_t)(U.p0 + ch + n) * a.d + m] = v[n];
+                    if (a.ssq != nullptr) {
+                        // sum of y^2 over the unit's 128 rows for every pick of the
+                        // chunk: a reduce-scatter across the warp (lane l ends with
+                        // pick idx), then (below) the four warps' sums in warp order
+                        float q[EC];
+#pragma unroll
+                        for (int n = 0; n < EC; ++n) q[n] = v[n] * v[n];
+                        int idx = 0;
+#pragma unroll
+                        for (int step = 0; step < 5; ++step) {
+                            const int o = 16 >> step;
+                            const int c = EC >> step;       // values a lane holds before this step
+                            const bool hi = (lane & o) != 0;
+                            if (c > 1) {
+#pragma unroll
+                                for (int j = 0; j < c / 2; ++j) {
+                                    const float send = hi ? q[j] : q[j + c / 2];
+                                    const float keep = hi ? q[j + c / 2] : q[j];
+                                    q[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                                }
+                                idx += hi ? c / 2 : 0;
+                            } else {
+                                q[0] += __shfl_xor_sync(0xffffffffu, q[0], o);
+                            }
+                        }
+                        // every pick's sum now sits on 32 / EC lanes
+                        float* part = xch;                             // [4][NTT]
+                        if ((lane & (32 / EC - 1)) == 0) part[qd * NTT + ch + idx] = q[0];
+                    }
                 }
+            }
+            if (!U.down) {
+                if (r < 64) ptx::fence_proxy_async_global();
                 ptx::named_bar_sync(1, 128);
                 if (warp == EPI_WARP0 && lane == 0) {
                     __threadfence();
                     ptx::red_release_gpu_add(&a.tile_ready[U.tile], 1u);
                 }
-            } else {
-                const int m = U.mb * AROWS + r;
-#pragma unroll
-                for (int n = 0; n < NTT; ++n)
-                    if (n < U.n) a.y[(size_t)(U.p0 + n) * a.d + m] = v[n];
-                if (a.ssq != nullptr) {
-                    // sum of y^2 over the unit's 128 rows for every pick: a
-                    // reduce-scatter across the warp (lane l ends with pick idx),
-                    // then the four warps' sums in warp order
-                    float q[NTT];
-#pragma unroll
-                    for (int n = 0; n < NTT; ++n) q[n] = v[n] * v[n];
-                    int idx = 0;
-#pragma unroll
-                    for (int step = 0; step < 5; ++step) {
-                        const int o = 16 >> step;
-                        const int c = NTT >> step;      // values a lane holds before this step
-                        const bool hi = (lane & o) != 0;
-                        if (c > 1) {
-#pragma unroll
-                            for (int j = 0; j < c / 2; ++j) {
-                                const float send = hi ? q[j] : q[j + c / 2];
-                                const float keep = hi ? q[j + c / 2] : q[j];
-                                q[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
-                            }
-                            idx += hi ? c / 2 : 0;
-                        } else {
-                            q[0] += __shfl_xor_sync(0xffffffffu, q[0], o);
-                        }
-                    }
-                    // every pick's sum now sits on 32 / NTT lanes
-                    float* part = xch;                             // [4][NTT]
-                    if ((lane & (32 / NTT - 1)) == 0) part[qd * NTT + idx] = q[0];
-                    ptx::named_bar_sync(1, 128);
-                    if (r < U.n)
-                        a.ssq[(size_t)(U.p0 + r) * (a.d / AROWS) + U.mb] =
-                            ((part[r] + part[NTT + r]) + part[2 * NTT + r]) + part[3 * NTT + r];
-                }
+            } else if (a.ssq != nullptr) {
+                const float* part = xch;
+                ptx::named_bar_sync(1, 128);
+                for (int pr = r; pr < U.n; pr += 128)
+                    a.ssq[(size_t)(U.p0 + pr) * (a.d / AROWS) + U.mb] =
+                        ((part[pr] + part[NTT + pr]) + part[2 * NTT + pr]) + part[3 * NTT + pr];
             }
         }
     }
@@ -817,8 +840,10 @@ cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p,
         e = stma ? launch_mx<true, 8>(s, L, p, st) : launch_mx<false, 8>(s, L, p, st);
     else if (L.nt == 16)
         e = stma ? launch_mx<true, 16>(s, L, p, st) : launch_mx<false, 16>(s, L, p, st);
-    else
+    else if (L.nt == 32)
         e = stma ? launch_mx<true, 32>(s, L, p, st) : launch_mx<false, 32>(s, L, p, st);
+    else
+        e = stma ? launch_mx<true, 64>(s, L, p, st) : launch_mx<false, 64>(s, L, p, st);
     timing_end(st);
     return e;
 }

@@ -18,6 +18,7 @@ static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 int tile_picks(const moe_shape& s) {
     const int64_t picks = (int64_t)s.S * s.k;
     if (picks <= 2 * (int64_t)s.E) return 8;
+    if (picks >= 64 * (int64_t)s.E) return 64;
     return picks >= 32 * (int64_t)s.E ? 32 : 16;
 }
 

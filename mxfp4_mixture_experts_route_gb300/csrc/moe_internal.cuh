@@ -30,9 +30,9 @@ static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
 
 // Token-tile width of the expert GEMMs: one tile holds up to nt picks of one
 // expert (an MMA N of 2 nt: hi and lo row per pick), nt = 16 (the pages'
-// 16-row tiles, k5 page), 8 when the call's experts get few picks each, 32
-// when they get many.
-constexpr int NT_MAX = 32;
+// 16-row tiles, k5 page), 8 when the call's experts get few picks each, 32 or
+// 64 when they get many.
+constexpr int NT_MAX = 64;
 int tile_picks(const moe_shape& s);
 
 // Block scales of the gathered tokens and of h (e8m0, one per 32 elements):

@@ -329,6 +329,13 @@ __device__ __forceinline__ void tmem_st2(uint32_t taddr, uint32_t v0, uint32_t v
     asm volatile("tcgen05.st.sync.aligned.32x32b.x2.b32 [%0], {%1, %2};" ::"r"(taddr), "r"(v0), "r"(v1) : "memory");
 }
 
+// 32 lanes x 4 consecutive 32-bit TMEM columns (taddr's column a multiple of 4)
+__device__ __forceinline__ void tmem_st4(uint32_t taddr, uint32_t v0, uint32_t v1, uint32_t v2, uint32_t v3) {
+    asm volatile("tcgen05.st.sync.aligned.32x32b.x4.b32 [%0], {%1, %2, %3, %4};" ::"r"(taddr), "r"(v0), "r"(v1),
+                 "r"(v2), "r"(v3)
+                 : "memory");
+}
+
 // 32 lanes x 4 consecutive 32-bit TMEM columns, all four set to v (taddr's
 // column a multiple of 4)
 __device__ __forceinline__ void tmem_st4_rep(uint32_t taddr, uint32_t v) {
