@@ -73,7 +73,7 @@ constexpr int A_TX = AROWS * KS / 2;         // packed bytes of a weight tile: t
 #define MOE_MX_TOKEN_STAGES 4
 #endif
 #ifndef MOE_MX_WIDE_TOKEN_STAGES
-#define MOE_MX_WIDE_TOKEN_STAGES 2
+#define MOE_MX_WIDE_TOKEN_STAGES 3
 #endif
 constexpr int NSB_DEF = MOE_MX_TOKEN_STAGES; // token-tile stages (two for 64-pick tiles)
 constexpr int TMEM_COLS = 512;

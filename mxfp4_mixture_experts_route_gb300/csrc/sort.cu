@@ -257,8 +257,9 @@ cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs
 }
 
 bool topk_sort_fits(const moe_shape& s) {
-    // at most 4 tokens a warp, and the ids of the call in shared memory
-    return s.S <= 4 * (SORT_THREADS / 32) && (size_t)s.S * s.k <= 8192;
+    // one token a warp (beyond that the top-k kernel spreads the tokens over
+    // more SMs), and the ids of the call in shared memory
+    return s.S <= SORT_THREADS / 32 && (size_t)s.S * s.k <= 8192;
 }
 
 cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
