@@ -22,8 +22,7 @@ constexpr int CB_MAXK = 16;               // picks per token (k <= 16)
 // writes: warp w adds up the blocks of picks w and w + 8 (lanes over blocks,
 // then a fixed shuffle tree), so the CTA never reads a whole y row twice.
 // y rows are addressed through pos[t*k + j] (the sorted per-pick buffer).
-__global__ void __launch_bounds__(CB_THREADS) k_combine(const float* __restrict__ y, const float* __restrict__ ssq,
-                                                        const int32_t* __restrict__ pos, const float* __restrict__ w,
+__global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const float* ssq, const int32_t* pos, const float* w,
                                                         const float* __restrict__ norm_w, float eps, int k, int d,
                                                         float* __restrict__ out) {
     pdl_trigger();
@@ -36,15 +35,15 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* __restrict_
     for (int h = 0; h < CB_MAXK / 8; ++h) {
         const int j = warp + 8 * h;
         if (j < k) {
-            const int p = pos[(size_t)t * k + j];
-            float c = w[(size_t)t * k + j];
+            const int p = ld_dep(pos + (size_t)t * k + j);
+            float c = ld_dep(w + (size_t)t * k + j);
             if (norm_w != nullptr && p >= 0) {
                 const int nb = d / 128;                // <= 128 row blocks
                 float q = 0.f;
 #pragma unroll
                 for (int i = 0; i < 4; ++i) {
                     const int b = lane + 32 * i;
-                    if (b < nb) q += ssq[(size_t)p * nb + b];
+                    if (b < nb) q += ld_dep(ssq + (size_t)p * nb + b);
                 }
 #pragma unroll
                 for (int m = 16; m >= 1; m >>= 1) q += __shfl_xor_sync(0xffffffffu, q, m);
@@ -63,7 +62,7 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* __restrict_
 #pragma unroll
     for (int j = 0; j < CB_MAXK; ++j) {           // every pick's load in flight at once
         v[j] = make_float4(0.f, 0.f, 0.f, 0.f);
-        if (j < k && prow[j] >= 0) v[j] = *reinterpret_cast<const float4*>(y + (size_t)prow[j] * d + col);
+        if (j < k && prow[j] >= 0) v[j] = ld_dep(reinterpret_cast<const float4*>(y + (size_t)prow[j] * d + col));
     }
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
 #pragma unroll

@@ -147,6 +147,17 @@ struct Args {
     int max_tiles;
 };
 
+// A tile entry of the sort's table (an earlier kernel's output: read through L2)
+__device__ __forceinline__ Tile load_tile(const Tile* p) {
+    const int4 v = ld_dep(reinterpret_cast<const int4*>(p));
+    Tile t;
+    t.e = v.x;
+    t.p0 = v.y;
+    t.n = v.z;
+    t.pad = v.w;
+    return t;
+}
+
 struct Unit {
     int down;        // 0: gate_up, 1: down, -1: no more units
     int tile, mb;    // tile index and row block
@@ -261,8 +272,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     int claim1 = 0, n_tiles = 0;
     Tile tile0 = {0, 0, 0, 0};
     if (warp == SCHED_WARP) {
-        n_tiles = sb->n_tiles;
-        tile0 = a.tiles[min((int)blockIdx.x / (a.I / 64), a.max_tiles - 1)];
+        n_tiles = ld_dep(&sb->n_tiles);
+        tile0 = load_tile(a.tiles + min((int)blockIdx.x / (a.I / 64), a.max_tiles - 1));
         if (lane == 0) claim1 = atomicAdd(&sb->work_next, 1);   // raw counter value
     }
     ptx::tc_fence_before();
@@ -352,7 +363,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int u = (int)blockIdx.x;
         int next_claim = claim1;   // lane 0
         Tile tl = tile0, tl_next = {0, 0, 0, 0};
-        if (u >= U1 && u < total) tl = a.tiles[tile_of(u)];
+        if (u >= U1 && u < total) tl = load_tile(a.tiles + tile_of(u));
         for (int i = 0;; ++i) {
             Unit U;
             if (u < total) {
@@ -367,7 +378,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             U.pad = 0;
             const int u_next = u < total ? (int)gridDim.x + __shfl_sync(0xffffffffu, next_claim, 0) : total;
-            if (u_next < total) tl_next = a.tiles[tile_of(u_next)];
+            if (u_next < total) tl_next = load_tile(a.tiles + tile_of(u_next));
             if (lane == 0) next_claim = u_next < total ? atomicAdd(&sb->work_next, 1) : total;
             // publish unit i once the weight producer has taken unit i - LOOKAHEAD
             // (bounded): claimed units wait in this CTA for a short while only

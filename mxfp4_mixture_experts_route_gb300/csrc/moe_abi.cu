@@ -37,12 +37,9 @@ WsLayout ws_layout(const moe_shape& s) {
     // SM count only changes how the work is split
     L.router_kslices = router_kslices(s, 152);
     L.logits = take((size_t)s.S * s.E * 4);
-    L.counts = take((size_t)s.E * 4);
-    L.offsets = take((size_t)(s.E + 1) * 4);
     L.pos = take(P * 4);
     L.src = take(P * 4);
     L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
-    L.active = take((size_t)s.E * 4);
     L.tile_ready = take((size_t)L.max_tiles * 4);
     // e4m3 hi / lo rows of the gathered tokens and of h, and their block scales
     const size_t rows = P + NT_MAX;

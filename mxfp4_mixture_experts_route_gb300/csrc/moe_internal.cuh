@@ -21,10 +21,9 @@ struct StatusBlock {
     int32_t detail;     // code-specific detail of that error
     int32_t n_picks;    // valid picks of the current call (written by the sort)
     int32_t n_tiles;    // gate_up work tiles of the current call
-    int32_t n_active;   // experts with at least one pick
     int32_t work_next;  // persistent-kernel work counters (reset each call)
     int32_t work_next2;
-    int32_t pad[57];
+    int32_t pad[58];
 };
 static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
 
@@ -49,7 +48,7 @@ struct Tile {
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, logits, counts, offsets, pos, src, tiles, active, tile_ready, xq, xs, hq, hs, y, ssq;
+    size_t status, logits, pos, src, tiles, tile_ready, xq, xs, hq, hs, y, ssq;
     size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
     size_t total;
     int max_tiles;
@@ -74,17 +73,25 @@ __device__ __forceinline__ void latch_status(StatusBlock* sb, int code, int deta
 
 // ---------------------------------------------------------------------------
 // Programmatic dependent launch.  The block's kernels are launched so that the
-// next one may start while its predecessor is still running: every kernel
-// allows its successor to launch at once (pdl_trigger), does the work that
-// needs no predecessor's data, and calls pdl_wait, which returns when the
-// predecessor grid has completed and its writes are visible, before it reads
-// or writes anything the stream's earlier kernels touch.  Before the wait a
-// kernel reads only the caller's weights and bias, which none of the block's
-// kernels writes; a kernel of the caller's that precedes the block triggers
-// its successor only at exit, so the block never starts ahead of it.  Without
-// the launch attribute pdl_wait returns at once.
+// next one may start while its predecessor is still running: a kernel allows
+// its successor to launch (pdl_trigger), does the work that needs no
+// predecessor's data, and calls pdl_wait, which returns when the predecessor
+// grid has completed and its writes are visible, before it reads or writes
+// anything the stream's earlier kernels of the call touch.  The first kernel
+// of a call triggers only after its own wait has returned, i.e. once the
+// stream's work before the call (which wrote x) has completed; every later
+// kernel triggers at its start.  So before its wait a kernel may read the
+// call's inputs (weights, bias, x), which none of the block's kernels writes.
+// Without the launch attribute pdl_wait returns at once.
 // ---------------------------------------------------------------------------
 __device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+// Loads of what an earlier kernel of the call wrote go through L2 (ld.global.cg):
+// that kernel may still have been running when this one started, so the data
+// is not read-only for this kernel's lifetime, which the non-coherent path
+// (__ldg, or a const __restrict__ pointer the compiler may read that way)
+// requires; a stale line there was seen to survive the wait.
+template <typename T>
+__device__ __forceinline__ T ld_dep(const T* p) { return __ldcg(p); }
 __device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
 
 template <typename... KArgs, typename... Args>

@@ -54,7 +54,6 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
     const int k_begin = (int)((long long)nk * ks / kslices) * 128;
     const int k_end = (int)((long long)nk * (ks + 1) / kslices) * 128;
     const int nt = min(RT_TOKENS, S - t0);
-    pdl_trigger();
     float acc[RT_TOKENS];
 #pragma unroll
     for (int t = 0; t < RT_TOKENS; ++t) acc[t] = 0.f;
@@ -63,7 +62,10 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
         const int q16 = klen / 8;                            // 16-byte pieces of a row slice
         uint4 w = make_uint4(0, 0, 0, 0);
         if (e < E && lane < q16) w = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)e * d + kc) + lane);
-        if (kc == k_begin) pdl_wait();   // the first weight slice is in flight; x may come from the stream's last kernel
+        if (kc == k_begin) {
+            pdl_wait();      // the first weight slice is in flight; x may come from the stream's last kernel
+            pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
+        }
         __syncthreads();
         for (int i = threadIdx.x; i < nt * q16; i += RT_THREADS) {
             const int r = i / q16, c = i % q16;
@@ -131,7 +133,6 @@ __global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* 
     const int nk = d / 128;
     const int k_begin = (int)((long long)nk * ks / kslices) * 128;
     const int k_end = (int)((long long)nk * (ks + 1) / kslices) * 128;
-    pdl_trigger();
     uint4 w[NR];
     int q16[NR];
 #pragma unroll
@@ -141,7 +142,8 @@ __global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* 
         w[r] = make_uint4(0, 0, 0, 0);
         if (e < E && lane < q16[r]) w[r] = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)e * d + kc) + lane);
     }
-    pdl_wait();   // x may come from the stream's previous kernel
+    pdl_wait();      // x may come from the stream's previous kernel
+    pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
     uint4 xv[NR][NTOK];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
@@ -193,7 +195,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* 
 }
 
 // One warp per token (see topk_token).
-__global__ void __launch_bounds__(256) k_topk(const float* __restrict__ L, const float* __restrict__ bias,
+__global__ void __launch_bounds__(256) k_topk(const float* L, const float* __restrict__ bias,
                                               int S, int E, int k, int32_t* __restrict__ ids,
                                               float* __restrict__ wout) {
     const int lane = threadIdx.x & 31;

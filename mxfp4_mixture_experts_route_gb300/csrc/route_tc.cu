@@ -54,7 +54,6 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     const int e0 = blockIdx.x * RM, t0 = blockIdx.y * RN, ks = blockIdx.z;
     const int nk = d / RK;
     const int kb = (int)((long long)nk * ks / kslices), ke = (int)((long long)nk * (ks + 1) / kslices);
-    pdl_trigger();
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
             ptx::mbar_init(&full[i], 1);
@@ -73,7 +72,8 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *holder;
-    pdl_wait();   // x may come from the stream's previous kernel
+    pdl_wait();      // x may come from the stream's previous kernel
+    pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
 
     auto fail = [&](int site) {
         latch_status(sb, MOE_ERR_TIMEOUT, 100 + site);

@@ -21,12 +21,9 @@ namespace {
 constexpr int SORT_THREADS = 1024;
 
 struct SortOut {
-    int32_t* counts;
-    int32_t* offsets;
     int32_t* pos;
     int32_t* src;
     Tile* tiles;
-    int32_t* active;
     uint32_t* tile_ready;
     int max_tiles;
     int nt;               // picks per tile
@@ -47,9 +44,9 @@ __host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
 //      and writes tile entries (expert e, first pick, picks in the tile)
 // The order of the picks inside a segment is the order the atomics came in:
 // each pick is an independent column of the expert GEMMs, so the results do
-// not depend on it.  ids may be in global or shared memory.
-// Output: counts[E], offsets[E+1], pos[S*k], src[n_picks], tiles[n_tiles],
-// active[n_active] and n_picks / n_tiles / n_active; tile_ready[] zeroed.
+// not depend on it.  ids is the top-k kernel's output in global memory.
+// Output: pos[S*k], src[n_picks], tiles[n_tiles] and n_picks / n_tiles;
+// tile_ready[] zeroed.
 __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int k, const SortOut& o,
                                            int32_t* smem) {
     int32_t* cnt = smem;               // [E + 1] counts
@@ -74,9 +71,9 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
         bool ok = false;
         if (p < P) {
             const int t = p / k, j = p - t * k;
-            e = ids[p];
+            e = ld_dep(ids + p);
             ok = e >= 0 && e < E;
-            for (int q = 0; q < j && ok; ++q) ok = ids[(size_t)t * k + q] != e;
+            for (int q = 0; q < j && ok; ++q) ok = ld_dep(ids + (size_t)t * k + q) != e;
         }
         const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
         const int leader = __ffs(grp) - 1;
@@ -96,36 +93,30 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
 
     // 2 ----------------------------------------------------------------------
     if (warp == 0) {
-        // lane l scans experts [l*per, (l+1)*per); three exclusive scans at once
+        // lane l scans experts [l*per, (l+1)*per); two exclusive scans at once
         const int per = (E + 31) / 32;
         const int e0 = lane * per, e1 = min(E, e0 + per);
-        int sp = 0, st = 0, sa = 0;
+        int sp = 0, st = 0;
         for (int e = e0; e < e1; ++e) {
             const int n = cnt[e];
             sp += n;
             st += (n + nt - 1) / nt;
-            sa += n > 0 ? 1 : 0;
         }
-        int ip = sp, it = st, ia = sa;
+        int ip = sp, it = st;
 #pragma unroll
         for (int m = 1; m < 32; m <<= 1) {
             const int a = __shfl_up_sync(0xffffffffu, ip, m);
             const int b = __shfl_up_sync(0xffffffffu, it, m);
-            const int c = __shfl_up_sync(0xffffffffu, ia, m);
             if (lane >= m) {
                 ip += a;
                 it += b;
-                ia += c;
             }
         }
-        int rp = ip - sp, rt = it - st, ra = ia - sa;   // exclusive prefixes of this lane's run
+        int rp = ip - sp, rt = it - st;   // exclusive prefixes of this lane's run
         for (int e = e0; e < e1; ++e) {
             const int n = cnt[e];
             off[e] = rp;
             toff[e] = rt;
-            o.counts[e] = n;
-            o.offsets[e] = rp;
-            if (n > 0) o.active[ra++] = e;
             rp += n;
             rt += (n + nt - 1) / nt;
         }
@@ -133,10 +124,8 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
             off[E] = ip;
             toff[E] = it;
             tot_tiles = it;
-            o.offsets[E] = ip;
             sb->n_picks = ip;
             sb->n_tiles = it;
-            sb->n_active = ia;
             sb->work_next = 0;
             sb->work_next2 = 0;
         }
@@ -147,7 +136,7 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
     for (int p = warp * 32 + lane; p < P; p += SORT_THREADS) {
         const int r = o.pos[p];
         if (r >= 0) {
-            const int q = off[ids[p]] + r;
+            const int q = off[ld_dep(ids + p)] + r;
             o.pos[p] = q;
             o.src[q] = p;
         }
@@ -171,11 +160,100 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
     }
 }
 
-__global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict__ ids, int S, int E, int k,
+// The same outputs for P = S * k <= SORT_THREADS picks, by pairwise counting
+// in one CTA (three barriers, no global round trip).  With key_p = (e_p, p)
+// over the valid picks, a pick's position is r_p = #{q : key_q < key_p} =
+// lt + eqb, where lt = #{q : e_q < e_p} is the start of expert e_p's segment
+// and eqb = #{q < p : e_q = e_p} the pick's index inside it; the segment's
+// length is eqt = #{q : e_q = e_p}.  Tile starts are the positions with
+// eqb mod nt = 0, numbered in position order by a ballot scan.  Inside a
+// segment the picks keep their order p.  ids is in shared memory; smem holds
+// 2 P ints.
+__device__ __forceinline__ void sort_picks_small(const int32_t* ids, int S, int E, int k, const SortOut& o,
+                                                 int32_t* smem) {
+    constexpr int NONE = 0x7fffffff;
+    int32_t* key = smem;            // [P] expert of pick p, NONE if the pick is not valid
+    int32_t* start = key + S * k;   // [P] by position: (expert << 8 | picks) of the tile starting there, or -1
+    __shared__ int32_t wcnt[SORT_THREADS / 32];
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = S * k, nt = o.nt;
+    StatusBlock* sb = o.sb;
+
+    for (int i = tid; i < o.max_tiles; i += SORT_THREADS) o.tile_ready[i] = 0u;
+    int valid = 0;
+    if (tid < P) {
+        const int t = tid / k, j = tid - t * k;
+        const int e = ids[tid];
+        valid = e >= 0 && e < E;
+        for (int q = 0; q < j && valid; ++q) valid = ids[t * k + q] != e;
+        key[tid] = valid ? e : NONE;
+        start[tid] = -1;
+        if (!valid) {
+            o.pos[tid] = -1;
+            latch_status(sb, MOE_ERR_BAD_IDS, tid);
+        }
+    }
+    const int n_valid = __syncthreads_count(valid);
+
+    // G threads (a power of two, at most a warp) count for one pick
+    int G = 32;
+    while (G > 1 && G * P > SORT_THREADS) G >>= 1;
+    const int p = tid / G, c = tid & (G - 1);
+    const int ep = p < P ? key[p] : NONE;
+    int lt = 0, eqb = 0, eqt = 0;
+    if (ep != NONE) {
+        for (int q = c; q < P; q += G) {
+            const int eq = key[q];
+            lt += eq < ep ? 1 : 0;
+            eqt += eq == ep ? 1 : 0;
+            eqb += (eq == ep && q < p) ? 1 : 0;
+        }
+    }
+    for (int m = 1; m < G; m <<= 1) {
+        lt += __shfl_xor_sync(0xffffffffu, lt, m);
+        eqt += __shfl_xor_sync(0xffffffffu, eqt, m);
+        eqb += __shfl_xor_sync(0xffffffffu, eqb, m);
+    }
+    if (c == 0 && ep != NONE) {
+        const int r = lt + eqb;
+        o.pos[p] = r;
+        o.src[r] = p;
+        if (eqb % nt == 0) start[r] = ep << 8 | min(nt, eqt - eqb);
+    }
+    __syncthreads();
+
+    // tile numbers: tile starts counted in position order
+    const int st = tid < n_valid ? start[tid] : -1;
+    const uint32_t bal = __ballot_sync(0xffffffffu, st >= 0);
+    if (lane == 0) wcnt[warp] = __popc(bal);
+    __syncthreads();
+    int before = 0, total = 0;
+    for (int w = 0; w < SORT_THREADS / 32; ++w) {
+        const int n = wcnt[w];
+        before += w < warp ? n : 0;
+        total += n;
+    }
+    if (st >= 0) {
+        Tile tl;
+        tl.e = st >> 8;
+        tl.p0 = tid;
+        tl.n = st & 255;
+        tl.pad = 0;
+        o.tiles[before + __popc(bal & ((1u << lane) - 1u))] = tl;
+    }
+    if (tid == 0) {
+        sb->n_picks = n_valid;
+        sb->n_tiles = total;
+        sb->work_next = 0;
+        sb->work_next2 = 0;
+    }
+}
+
+__global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* ids, int S, int E, int k,
                                                        SortOut o) {
     extern __shared__ int32_t smem[];
-    pdl_trigger();
     pdl_wait();
+    pdl_trigger();   // after the wait: see launch_gather
     sort_picks(ids, S, E, k, o, smem);
 }
 
@@ -183,13 +261,13 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* __restrict
 // see topk_token) and the sort of its picks in one CTA.  The ids go to the
 // caller's buffer and, for the sort, to shared memory.
 template <int MAXE>
-__global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* __restrict__ L,
+__global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* L,
                                                             const float* __restrict__ bias, int S, int E, int k,
                                                             int32_t* __restrict__ ids,
                                                             float* __restrict__ weights, SortOut o) {
     extern __shared__ int32_t smem[];
     pdl_trigger();
-    int32_t* sids = smem + sort_smem_ints(E);   // [S][k]
+    int32_t* sids = smem + 2 * S * k;   // [S][k]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float b[MAXE];
     load_bias(bias, E, lane, b);   // an input of the call: read before the wait
@@ -198,34 +276,48 @@ __global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* __restr
         topk_token(L + (size_t)t * E, b, E, k, lane, sids + (size_t)t * k, weights + (size_t)t * k);
     __syncthreads();
     for (int i = threadIdx.x; i < S * k; i += SORT_THREADS) ids[i] = sids[i];
-    sort_picks(sids, S, E, k, o, smem);
+    sort_picks_small(sids, S, E, k, o, smem);
 }
 
-// Token rows of the expert GEMMs (see quantize_pick).  grid (max_picks),
-// blockDim = d / 8 rounded up to a warp (at most 1024), one pick a CTA.
+// Token rows of the expert GEMMs.  grid (S * k), one pick p = t * k + j a
+// CTA, blockDim = d / 8 rounded up to a warp (at most 1024): the CTA
+// quantises token t's row (quantize_chunk) before it waits for the sort --
+// x is an input of the call, final before the call's first kernel lets its
+// successors start -- and then writes it to the pick's sorted position.
+constexpr int GATHER_PASSES = 2;   // d <= 16384
 __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __restrict__ x,
-                                                      const int32_t* __restrict__ src, int k, int d, int I, int P,
+                                                      const int32_t* pos, int k, int d, int I, int P,
                                                       uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-                                                      uint8_t* __restrict__ hs,
-                                                      const StatusBlock* __restrict__ sb) {
+                                                      uint8_t* __restrict__ hs) {
     pdl_trigger();
+    const int p = blockIdx.x, t = p / k;
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    const int nc = d / 8;
+    QuantChunk q[GATHER_PASSES];
+#pragma unroll
+    for (int i = 0; i < GATHER_PASSES; ++i) {
+        const int c = i * (int)blockDim.x + (int)threadIdx.x;
+        if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, c, c < nc);   // block-uniform condition
+    }
     pdl_wait();
-    const int p = blockIdx.x;
-    const int sp = src[p];                 // read beside n_picks: src has max_picks entries
-    if (p >= sb->n_picks) return;
-    quantize_pick(x, sp / k, p, d, I, (size_t)P + NT_MAX, xq, xs, hs, threadIdx.x, blockDim.x);
+    const int r = ld_dep(pos + p);
+    if (r < 0) return;   // not a valid pick
+    const size_t tab_rows = (size_t)P + NT_MAX;
+#pragma unroll
+    for (int i = 0; i < GATHER_PASSES; ++i) {
+        const int c = i * (int)blockDim.x + (int)threadIdx.x;
+        if (c < nc) store_chunk(q[i], c, r, d, tab_rows, xq, xs);
+    }
+    pad_scale_rows(r, d, I, tab_rows, xs, hs, threadIdx.x);
 }
 
 }  // namespace
 
 static SortOut sort_out(const WsLayout& L, char* ws) {
     SortOut o;
-    o.counts = reinterpret_cast<int32_t*>(ws + L.counts);
-    o.offsets = reinterpret_cast<int32_t*>(ws + L.offsets);
     o.pos = reinterpret_cast<int32_t*>(ws + L.pos);
     o.src = reinterpret_cast<int32_t*>(ws + L.src);
     o.tiles = reinterpret_cast<Tile*>(ws + L.tiles);
-    o.active = reinterpret_cast<int32_t*>(ws + L.active);
     o.tile_ready = reinterpret_cast<uint32_t*>(ws + L.tile_ready);
     o.max_tiles = L.max_tiles;
     o.nt = L.nt;
@@ -233,15 +325,18 @@ static SortOut sort_out(const WsLayout& L, char* ws) {
     return o;
 }
 
+// The gather reads x before its wait.  That is safe because the first kernel
+// of every call (the router, or the sort for moe_experts) lets its successors
+// start only after its own wait has returned, i.e. after the stream's work
+// before the call -- which wrote x -- has completed.
 static cudaError_t launch_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     char* ws = p.ws;
     timing_begin(K_GATHER, st);
     const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
-    const cudaError_t e = launch_pdl(k_quant_gather, dim3(L.max_picks), dim3(threads), 0, st, p.x,
-                                     reinterpret_cast<const int32_t*>(ws + L.src), s.k, s.d, s.I, L.max_picks,
+    const cudaError_t e = launch_pdl(k_quant_gather, dim3(s.S * s.k), dim3(threads), 0, st, p.x,
+                                     reinterpret_cast<const int32_t*>(ws + L.pos), s.k, s.d, s.I, L.max_picks,
                                      reinterpret_cast<uint8_t*>(ws + L.xq), reinterpret_cast<uint8_t*>(ws + L.xs),
-                                     reinterpret_cast<uint8_t*>(ws + L.hs),
-                                     reinterpret_cast<const StatusBlock*>(ws + L.status));
+                                     reinterpret_cast<uint8_t*>(ws + L.hs));
     timing_end(st);
     return e;
 }
@@ -258,12 +353,12 @@ cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs
 
 bool topk_sort_fits(const moe_shape& s) {
     // one token a warp (beyond that the top-k kernel spreads the tokens over
-    // more SMs), and the ids of the call in shared memory
-    return s.S <= SORT_THREADS / 32 && (size_t)s.S * s.k <= 8192;
+    // more SMs), and one thread a pick for the pairwise-count sort
+    return s.S <= SORT_THREADS / 32 && s.S * s.k <= SORT_THREADS;
 }
 
 cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    const size_t smem = ((size_t)sort_smem_ints(s.E) + (size_t)s.S * s.k) * sizeof(int32_t);
+    const size_t smem = (size_t)3 * s.S * s.k * sizeof(int32_t);   // ids, keys, tile starts
     auto kern = s.E <= 256 ? k_topk_sort<256 / 32> : k_topk_sort<512 / 32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;

@@ -59,14 +59,14 @@ __device__ __forceinline__ void load_bias(const float* __restrict__ bias, int E,
 // retire it and find its next best.  Writes ids_out[0..k) in ascending id and
 // w_out[0..k).
 template <int MAXE>
-__device__ __forceinline__ void topk_token(const float* __restrict__ Lrow, const float (&b)[MAXE], int E, int k,
+__device__ __forceinline__ void topk_token(const float* Lrow, const float (&b)[MAXE], int E, int k,
                                            int lane, int32_t* ids_out, float* w_out) {
     float s[MAXE], z[MAXE];
     uint32_t key[MAXE];
 #pragma unroll
     for (int i = 0; i < MAXE; ++i) {           // independent loads, all in flight together
         const int e = lane + 32 * i;
-        z[i] = e < E ? Lrow[e] : 0.f;
+        z[i] = e < E ? ld_dep(Lrow + e) : 0.f;   // the router's output
     }
 #pragma unroll
     for (int i = 0; i < MAXE; ++i) {
