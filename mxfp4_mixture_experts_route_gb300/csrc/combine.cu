@@ -1,7 +1,7 @@
 // Per-pick post-expert norm and weighted combine.
 //
-// vllm.models.muse_spark.amd.mono.kernels.k3, stage E: "per-pick post-expert
-// norm and weighted sum".  On one GPU with every expert resident there is no
+// vllm.models.muse_spark.amd.mono.kernels.k3, stage E (a norm of each pick's
+// expert output, then the weighted sum).  On one GPU with every expert resident there is no
 // EP partial to reduce-scatter: the weighted sum over a token's k picks is the
 // block's output, out[t] = sum_j w_j * [RMSNorm](y_{t,j}), summed in pick
 // order j (ascending expert id for ids from moe_route).

@@ -2,8 +2,8 @@
 // scaling: one persistent kernel runs every gate_up unit and then every down
 // unit of the call.
 //
-// vllm.models.muse_spark.amd.mono.kernels.k3, stages C, D: "gate_up / down of
-// the local experts: MXFP4 weights ...": the weights stay in their MX form,
+// vllm.models.muse_spark.amd.mono.kernels.k3, stages C and D (the local
+// experts' gate_up and down projections on MXFP4 weights): the weights stay in their MX form,
 // e2m1 codes with one e8m0 scale per 32 elements of a row; fp4_mma: a 256-K
 // chunk of a row group per step; task_ring: compute the current task with the
 // next tasks' loads in flight.  vllm.models.kimi_k3.amd.specialized_decode.

@@ -1,19 +1,19 @@
 // Router logits (fp32) and sigmoid top-k.
 //
-// vllm.models.muse_spark.amd.mono.kernels.k3, stage A: "router logits (fp32)";
-// stage route: every token's top-8; route_token: "sigmoid + ..." over a wave's
-// tokens.  vllm.models.muse_spark.amd.mono.kernels.k5, HA: "router (fp32) ...
-// top-8 (CTA t routes token t) ... top-k ids / weights".
-// vllm.models.kimi_k3.amd.specialized_decode.mono.layer, k2_launch: w_gate and
-// an fp32 bias.
+// vllm.models.muse_spark.amd.mono.kernels.k3, stage A (the router's logits in
+// fp32), stage route (every token's top 8) and route_token (a sigmoid score per
+// expert, over a wave's tokens); vllm.models.muse_spark.amd.mono.kernels.k5,
+// stage HA (fp32 router, top 8 with one CTA per token, ids and weights handed
+// to the next stage); vllm.models.kimi_k3.amd.specialized_decode.mono.layer,
+// k2_launch (the router weight w_gate and an fp32 bias).
 //
 // GB300 design: the pages split the router's K over 8-CTA groups of a rank and
 // all-gather the partial logits; on one GPU the logits are one [S, d] x [d, E]
 // product.  It is split over CTAs by 8 experts x 32 tokens, and when that
 // leaves SMs idle, over K as well: the K-ranges of one output tile run as one
 // thread-block cluster and are added up in the cluster's shared memory in a
-// fixed order.  One warp a token then does the selection (the k3 "every CTA
-// routes every token" redundancy is not needed: the ids are produced once).
+// fixed order.  One warp a token then does the selection (k3 repeats the
+// routing in every CTA; here the ids are produced once and read by the sort).
 #include "moe_internal.cuh"
 #include "topk.cuh"
 

@@ -1,7 +1,7 @@
 // Router logits on the tensor cores, for batches of 64 tokens and more.
 //
-// vllm.models.muse_spark.amd.mono.kernels.k3, stage A: "router logits (fp32)";
-// the pages split the router's K over 8-CTA groups.  At larger batches the
+// vllm.models.muse_spark.amd.mono.kernels.k3, stage A (the router's logits in
+// fp32); the pages split the router's K over 8-CTA groups.  At larger batches the
 // logits are a dense [E, d] x [d, S] product, so here they are one: M = 128
 // experts x N = 128 tokens per tile, tcgen05.mma kind::f16 (bf16 x bf16, fp32
 // accumulate in TMEM; each product is exact in fp32), both operands by TMA in

@@ -1,8 +1,8 @@
 // Sigmoid top-k of one token by one warp (shared by the top-k kernel and the
 // fused top-k + sort kernel).
 //
-// vllm.models.muse_spark.amd.mono.kernels.k3, route_token: "sigmoid + ...";
-// k5, HA: "top-8 ... top-k ids / weights".  s = sigmoid(L), sel = s + bias;
+// vllm.models.muse_spark.amd.mono.kernels.k3, route_token (sigmoid scores);
+// k5, stage HA (top 8, ids and weights out).  s = sigmoid(L), sel = s + bias;
 // the k largest sel win (ties -> lower expert id), reported in ascending id
 // order with w_j = s_j / sum of the picks' s.
 #pragma once

@@ -7,14 +7,14 @@ input generator ``moe_inputs``, which holds no arithmetic of the block).
 
 Everything here is the plain definition of the block, evaluated in fp64, with
 one exception that the pages fix: the router logits are fp32 values (the k3
-page, stage A: "router logits (fp32)").  They are formed as the exact fp64 dot
+page, stage A, gives the router's logits in fp32).  They are formed as the exact fp64 dot
 product rounded once to fp32.
 
 Pages cited (vLLM API documentation):
   k3  = vllm.models.muse_spark.amd.mono.kernels.k3 -- stage list (A, route,
         C/D, E) and the summaries of route_token, mx_chunk, fp4_mma, dn_loads.
-  k5  = vllm.models.muse_spark.amd.mono.kernels.k5 -- HA: "router (fp32) ...
-        top-8 ... h, top-k ids / weights for HM".
+  k5  = vllm.models.muse_spark.amd.mono.kernels.k5 -- stage HA: fp32 router,
+        top 8, ids and weights handed to the expert stage.
   k2  = vllm.models.kimi_k3.amd.specialized_decode.mono.layer -- K2b's latent
         MoE and the k2_launch argument list (w_gate, bias, w13, w13s, w2, w2s,
         out [S, 7168]).
@@ -126,8 +126,8 @@ def routing_scores(L32: np.ndarray, bias: np.ndarray) -> tuple[np.ndarray, np.nd
 
 
 def route(L32: np.ndarray, bias: np.ndarray, k: int) -> tuple[np.ndarray, np.ndarray]:
-    """Sigmoid top-k (k3 route_token "sigmoid + ..."; k5 "top-8 ... top-k ids /
-    weights").  Returns ids [S, k] int32 in ascending expert order and the
+    """Sigmoid top-k (k3 route_token: sigmoid scores; k5 stage HA: top 8, ids
+    and weights).  Returns ids [S, k] int32 in ascending expert order and the
     renormalised weights [S, k] fp64."""
     s, sel = routing_scores(L32, bias)
     S, E = s.shape
@@ -175,7 +175,7 @@ def expert_ffn(xf: np.ndarray, w13: np.ndarray, w13s: np.ndarray,
 
 
 def post_expert_norm(y: np.ndarray, norm_w: np.ndarray, eps: float) -> np.ndarray:
-    """Per-pick RMSNorm of an expert output (k3 stage E, "per-pick post-expert norm")."""
+    """Per-pick RMSNorm of an expert output (k3 stage E: a norm of each pick's output)."""
     ms = np.mean(y * y, axis=-1, keepdims=True)
     return y / np.sqrt(ms + eps) * np.asarray(norm_w, np.float64)
 
