@@ -175,14 +175,17 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate,
                 void* ws, size_t ws_bytes, void* stream);
 
 /*
- * moe_forward with the step's input and outputs in HOST memory:
- *   x_host [S, d] bf16 is copied to the device inside the workspace, the block
- *   runs, and ids_host [S, k], weights_host [S, k], out_host [S, d] are copied
- *   back, all enqueued on `stream` (cudaMemcpyAsync; pinned host memory makes
- *   them asynchronous).  The weights (w_gate, bias, logit_off, w13, w13s, w2,
- *   w2s, norm_w) stay device pointers.  The host buffers must not be touched
- *   until the stream has been synchronised.  ids_host / weights_host may be
- *   NULL (then only out is copied back).
+ * moe_forward with the step's input and outputs in HOST memory: x_host [S, d]
+ * bf16 in, ids_host [S, k], weights_host [S, k], out_host [S, d] out, all
+ * enqueued on `stream`.  A small pinned buffer the GPU can address
+ * (cudaHostAlloc'd or cudaHostRegister'ed memory; on GB300 over the coherent
+ * CPU-GPU link) is read or written in place by the kernels and must then be
+ * 16-byte aligned (MOE_ERR_ALIGNMENT otherwise): x when S <= 8, ids and weights
+ * when S <= 32 and S * k <= 1024, out when S * d * 4 <= 256 KiB.  Every other
+ * host buffer is staged through the workspace with one cudaMemcpyAsync.  The weights (w_gate,
+ * bias, logit_off, w13, w13s, w2, w2s, norm_w) stay device pointers.  The host
+ * buffers must not be touched until the stream has been synchronised.
+ * ids_host / weights_host may be NULL (then only out is returned).
  */
 int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_gate,
                      const float* bias, const float* logit_off,

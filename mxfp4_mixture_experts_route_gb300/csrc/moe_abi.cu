@@ -249,6 +249,24 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate, const
     return run_forward(*shape, L, p, (cudaStream_t)stream);
 }
 
+}  // extern "C"
+
+namespace {
+// The device address of a pinned host buffer the GPU reads and writes in place
+// (cudaHostAlloc'd or registered memory under unified addressing; on GB300 over
+// the coherent CPU-GPU link), else nullptr: pageable memory is staged.
+void* device_view(const void* host) {
+    cudaPointerAttributes at;
+    if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
+        cudaGetLastError();
+        return nullptr;
+    }
+    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+}
+}  // namespace
+
+extern "C" {
+
 int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_gate, const float* bias,
                      const float* logit_off, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
                      const uint8_t* w2s, const float* norm_w, int32_t* ids_host, float* weights_host,
@@ -264,25 +282,40 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     rc = check_ws(shape, ws, ws_bytes);
     if (!rc) rc = check_device();
     if (rc) return rc;
-    // device copies of the step's input and outputs live in the workspace's
-    // host-I/O staging regions (xin, hio_ids, hio_w, hio_out)
+    // A small pinned host buffer is read or written in place by the kernels
+    // (measured faster than a copy): x when the router reads all of it in one
+    // round of loads (S <= 8), ids and weights when only the fused top-k +
+    // sort writes them and nothing reads them back, out up to 256 KB.  Every
+    // other buffer goes through the workspace's host-I/O staging regions
+    // (xin, hio_ids, hio_w, hio_out) and one copy, which moves bulk data
+    // faster than the kernels' own loads and stores over the link.
     WsLayout L = ws_layout(*shape);
     cudaStream_t st = (cudaStream_t)stream;
     char* w = (char*)ws;
     const size_t P = (size_t)shape->S * shape->k;
-    void* x_dev = w + L.xin;
-    rc = cuda_rc(cudaMemcpyAsync(x_dev, x_host, (size_t)shape->S * shape->d * 2, cudaMemcpyHostToDevice, st));
-    if (rc) return rc;
-    int32_t* ids_dev = (int32_t*)(w + L.hio_ids);
-    float* wts_dev = (float*)(w + L.hio_w);
-    float* out_dev = (float*)(w + L.hio_out);
+    const bool small_out = (size_t)shape->S * shape->d * 4 <= (256u << 10);
+    void* x_dev = shape->S <= 8 ? device_view(x_host) : nullptr;
+    int32_t* ids_dev = ids_host && topk_sort_fits(*shape) ? (int32_t*)device_view(ids_host) : nullptr;
+    float* wts_dev = weights_host && topk_sort_fits(*shape) ? (float*)device_view(weights_host) : nullptr;
+    float* out_dev = small_out ? (float*)device_view(out_host) : nullptr;
+    const bool ids_staged = !ids_dev, wts_staged = !wts_dev, out_staged = !out_dev;
+    if (!ids_dev) ids_dev = (int32_t*)(w + L.hio_ids);
+    if (!wts_dev) wts_dev = (float*)(w + L.hio_w);
+    if (!out_dev) out_dev = (float*)(w + L.hio_out);
+    if (!x_dev) {
+        x_dev = w + L.xin;
+        rc = cuda_rc(cudaMemcpyAsync(x_dev, x_host, (size_t)shape->S * shape->d * 2, cudaMemcpyHostToDevice, st));
+        if (rc) return rc;
+    }
+    if (!a16(x_dev) || !a16(out_dev) || !a16(ids_dev) || !a16(wts_dev)) return MOE_ERR_ALIGNMENT;
     rc = moe_forward(shape, x_dev, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids_dev, wts_dev,
                      out_dev, ws, ws_bytes, stream);
     if (rc) return rc;
-    rc = cuda_rc(cudaMemcpyAsync(out_host, out_dev, (size_t)shape->S * shape->d * 4, cudaMemcpyDeviceToHost, st));
-    if (!rc && ids_host)
+    if (out_staged)
+        rc = cuda_rc(cudaMemcpyAsync(out_host, out_dev, (size_t)shape->S * shape->d * 4, cudaMemcpyDeviceToHost, st));
+    if (!rc && ids_host && ids_staged)
         rc = cuda_rc(cudaMemcpyAsync(ids_host, ids_dev, P * 4, cudaMemcpyDeviceToHost, st));
-    if (!rc && weights_host)
+    if (!rc && weights_host && wts_staged)
         rc = cuda_rc(cudaMemcpyAsync(weights_host, wts_dev, P * 4, cudaMemcpyDeviceToHost, st));
     return rc;
 }

@@ -163,16 +163,24 @@ def test_scale_range(shift13, shift2):
     _check(inp, ids, w, out)
 
 
-def test_forward_host_matches_forward():
+@pytest.mark.parametrize("ci,pinned", [(1, True), (1, False), (2, True), (3, True)])
+def test_forward_host_matches_forward(ci, pinned):
+    """Host buffers: small pinned ones are read and written in place by the
+    kernels (all four at S = 8, ids and weights at S = 32), the others are
+    staged through the workspace; either way the bytes equal moe_forward's."""
     import torch
-    inp = mi.make_inputs(mi.CONFIGS[1])
+    inp = mi.make_inputs(mi.CONFIGS[ci])
     blk = device_block(inp)
     ids, w, out = [t.cpu().numpy() for t in blk.forward()]
     s = blk.shape
-    xh = torch.as_tensor(inp.x).view(torch.bfloat16).pin_memory()
-    oh = torch.empty((s.S, s.d), dtype=torch.float32).pin_memory()
-    ih = torch.empty((s.S, s.k), dtype=torch.int32).pin_memory()
-    wh = torch.empty((s.S, s.k), dtype=torch.float32).pin_memory()
+
+    def host(t):
+        return t.pin_memory() if pinned else t
+
+    xh = host(torch.as_tensor(inp.x).view(torch.bfloat16).clone())
+    oh = host(torch.empty((s.S, s.d), dtype=torch.float32))
+    ih = host(torch.empty((s.S, s.k), dtype=torch.int32))
+    wh = host(torch.empty((s.S, s.k), dtype=torch.float32))
     moe.forward_host(s, xh, blk.w_gate, blk.bias, blk.logit_off, blk.w13, blk.w13s, blk.w2, blk.w2s,
                      blk.norm_w, ih, wh, oh, blk.ws)
     torch.cuda.current_stream().synchronize()
