@@ -38,7 +38,6 @@ WsLayout ws_layout(const moe_shape& s) {
     L.router_kslices = router_kslices(s, 152);
     L.logits = take((size_t)s.S * s.E * 4);
     L.pos = take(P * 4);
-    L.src = take(P * 4);
     L.tiles = take((size_t)L.max_tiles * sizeof(Tile));
     L.tile_ready = take((size_t)L.max_tiles * 4);
     // e4m3 hi / lo rows of the gathered tokens and of h, and their block scales

@@ -48,7 +48,7 @@ struct Tile {
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, logits, pos, src, tiles, tile_ready, xq, xs, hq, hs, y, ssq;
+    size_t status, logits, pos, tiles, tile_ready, xq, xs, hq, hs, y, ssq;
     size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
     size_t total;
     int max_tiles;

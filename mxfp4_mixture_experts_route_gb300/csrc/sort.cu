@@ -22,7 +22,6 @@ constexpr int SORT_THREADS = 1024;
 
 struct SortOut {
     int32_t* pos;
-    int32_t* src;
     Tile* tiles;
     uint32_t* tile_ready;
     int max_tiles;
@@ -40,12 +39,12 @@ __host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
 //      atomic); the others get pos[p] = -1 and latch MOE_ERR_BAD_IDS
 //   2. one warp scans the counts over the experts: segment offsets, tile
 //      offsets and active-expert slots
-//   3. every thread places its picks (pos[p] = offset[e] + rank, src[pos] = p)
+//   3. every thread places its picks (pos[p] = offset[e] + rank)
 //      and writes tile entries (expert e, first pick, picks in the tile)
 // The order of the picks inside a segment is the order the atomics came in:
 // each pick is an independent column of the expert GEMMs, so the results do
 // not depend on it.  ids is the top-k kernel's output in global memory.
-// Output: pos[S*k], src[n_picks], tiles[n_tiles] and n_picks / n_tiles;
+// Output: pos[S*k], tiles[n_tiles] and n_picks / n_tiles;
 // tile_ready[] zeroed.
 __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int k, const SortOut& o,
                                            int32_t* smem) {
@@ -138,7 +137,6 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
         if (r >= 0) {
             const int q = off[ld_dep(ids + p)] + r;
             o.pos[p] = q;
-            o.src[q] = p;
         }
     }
     const int n_tiles = tot_tiles;
@@ -217,7 +215,6 @@ __device__ __forceinline__ void sort_picks_small(const int32_t* ids, int S, int 
     if (c == 0 && ep != NONE) {
         const int r = lt + eqb;
         o.pos[p] = r;
-        o.src[r] = p;
         if (eqb % nt == 0) start[r] = ep << 8 | min(nt, eqt - eqb);
     }
     __syncthreads();
@@ -316,7 +313,6 @@ __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __re
 static SortOut sort_out(const WsLayout& L, char* ws) {
     SortOut o;
     o.pos = reinterpret_cast<int32_t*>(ws + L.pos);
-    o.src = reinterpret_cast<int32_t*>(ws + L.src);
     o.tiles = reinterpret_cast<Tile*>(ws + L.tiles);
     o.tile_ready = reinterpret_cast<uint32_t*>(ws + L.tile_ready);
     o.max_tiles = L.max_tiles;
