@@ -37,8 +37,8 @@ __host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
 //   1. every pick p = t*k + j whose id e is in [0, E) and not repeated by an
 //      earlier pick of token t takes a rank within expert e (a shared-memory
 //      atomic); the others get pos[p] = -1 and latch MOE_ERR_BAD_IDS
-//   2. one warp scans the counts over the experts: segment offsets, tile
-//      offsets and active-expert slots
+//   2. one warp scans the counts over the experts: segment offsets and tile
+//      offsets
 //   3. every thread places its picks (pos[p] = offset[e] + rank)
 //      and writes tile entries (expert e, first pick, picks in the tile)
 // The order of the picks inside a segment is the order the atomics came in:
