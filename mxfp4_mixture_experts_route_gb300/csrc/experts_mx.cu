@@ -21,28 +21,32 @@
 // largest magnitude lands in [128, 256).  hi carries the leading 4 significant
 // bits and lo the next 4, so hi + lo is x / 2^s exactly for a bf16 x (to
 // within 2^-17 of the block maximum for elements more than 2^9 below it).
-// The MMA's N = 32 columns are the hi and lo rows of a 16-pick tile; the
-// epilogue adds each pick's two columns.
+// The MMA's N = 2 nt columns are the hi and lo rows of an nt-pick tile (nt =
+// 8, 16, 32 or 64, by the picks an expert gets on average); the epilogue adds
+// each pick's two columns.
 //
-// One persistent CTA per SM, 12 warps:
-//   warp 0      weight producer: per 256-K stage of a unit, the weight tile (128 rows x 256 K e2m1 =
-//               16 KB of HBM, 32 KB unpacked in shared memory; gate and up rows
-//               in one 4-D box) and its e8m0 bytes into a ring of weight stages.
-//   warp 7      token producer: the token tile (32 e4m3 rows x 256 K, one 3-D
-//               box of two 128-byte-swizzled slabs) and the tile's 16 rows of
-//               block scales (one bulk copy) into a ring of its own; for a
+// One persistent CTA per SM, 13 warps:
+//   warp 0      weight producer: per 256-K stage of a unit, the weight tile
+//               (128 rows x 256 K e2m1 = 16 KB of HBM, 32 KB in shared memory
+//               in the tensor core's 4-bit layout, which the tensor map writes;
+//               gate and up rows in one 4-D box) and its e8m0 bytes into a ring
+//               of weight stages.
+//   warp 7      token producer: the token tile (2 nt e4m3 rows x 256 K, one
+//               3-D box of two 128-byte-swizzled slabs) and the tile's nt rows
+//               of block scales (one bulk copy) into a ring of its own; for a
 //               down unit it first waits (bounded) for the tile's h.
 //   warps 8-11  scale movers: copy the stage's weight and token block scales
 //               from shared memory into TMEM, in the layout the MMA reads.
 //   warp 12     unit scheduler: claims units and reads their tile entries
 //               (global-memory round trips) at most LOOKAHEAD units ahead of the
 //               weight producer, and publishes them in the CTA's unit ring.
-//   warps 1-2   MMA issuers (lane 0 of each): M = 128 weight rows, N = 32,
+//   warps 1-2   MMA issuers (lane 0 of each): M = 128 weight rows, N = 2 nt,
 //               K = 32; issuer m takes the stages of parity m of every unit
-//               into an fp32 accumulator of its own (double buffered by unit).
-//               One thread needs several hundred cycles per stage for its
-//               waits, MMAs and commits, more than a stage lasts at full HBM
-//               bandwidth; two issuers on alternate stages keep up.
+//               into an fp32 accumulator of its own (buffered by unit).  One
+//               thread needs several hundred cycles per stage for its waits,
+//               MMAs and commits, more than a stage lasts at full HBM
+//               bandwidth; two issuers on alternate stages keep up (64-pick
+//               tiles, whose stages last longer, have one).
 //   warps 3-6   epilogue: the issuers' accumulators and each pick's hi and lo
 //               column added; h = silu(g) * u split into e4m3 hi/lo rows with a
 //               block scale per 32 rows for gate_up; y (fp32) and per-128-row
