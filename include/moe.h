@@ -49,7 +49,13 @@
  *     except per-device kernel attributes.
  *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
  *     stream).  Calls only enqueue work; they do not synchronise, except
- *     moe_device_status.
+ *     moe_device_status.  The library's kernels are launched with
+ *     programmatic dependent launch: later kernels of a call read its inputs
+ *     (weights, bias, x) before waiting on their predecessors, which is safe
+ *     because the call's first kernel lets them start only once the stream's
+ *     earlier work has completed.  A caller kernel launched the same way that
+ *     writes an input must therefore not signal launch completion before the
+ *     input is written.
  *   - `ws` is a device workspace of at least moe_workspace_bytes() bytes,
  *     256-byte aligned, prepared once with moe_workspace_init.  Its first
  *     bytes hold the device status word; calls that share one workspace must
