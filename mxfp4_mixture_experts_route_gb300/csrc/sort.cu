@@ -33,6 +33,16 @@ struct SortOut {
 // tile offset (E + 1 each)
 __host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
 
+// The pairwise-count sort (sort_picks_small) for up to SMALL_SORT_PICKS picks:
+// each thread then compares at most 16 keys for the pick it counts for; above
+// that the atomic-rank sort (sort_picks).  Shared memory of a sort kernel: the
+// chosen sort's ints, and the ids when they are staged there (always for the
+// pairwise count; for the atomic-rank sort only in the fused top-k + sort).
+constexpr int SMALL_SORT_PICKS = 128;
+__host__ __device__ constexpr int sort_smem_ints_for(int E, int P, bool ids_in_smem) {
+    return P <= SMALL_SORT_PICKS ? 3 * P : sort_smem_ints(E) + (ids_in_smem ? P : 0);
+}
+
 // Sort of the S * k picks by expert, one CTA of SORT_THREADS threads.
 //   1. every pick p = t*k + j whose id e is in [0, E) and not repeated by an
 //      earlier pick of token t takes a rank within expert e (a shared-memory
@@ -43,9 +53,17 @@ __host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
 //      and writes tile entries (expert e, first pick, picks in the tile)
 // The order of the picks inside a segment is the order the atomics came in:
 // each pick is an independent column of the expert GEMMs, so the results do
-// not depend on it.  ids is the top-k kernel's output in global memory.
+// not depend on it.  ids is in global memory (an earlier kernel's output, read
+// through L2) or, with SMEM_IDS, in shared memory.
 // Output: pos[S*k], tiles[n_tiles] and n_picks / n_tiles;
 // tile_ready[] zeroed.
+template <bool SMEM_IDS>
+__device__ __forceinline__ int id_at(const int32_t* ids, size_t i) {
+    if constexpr (SMEM_IDS) return ids[i];
+    else return ld_dep(ids + i);
+}
+
+template <bool SMEM_IDS>
 __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int k, const SortOut& o,
                                            int32_t* smem) {
     int32_t* cnt = smem;               // [E + 1] counts
@@ -70,9 +88,9 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
         bool ok = false;
         if (p < P) {
             const int t = p / k, j = p - t * k;
-            e = ld_dep(ids + p);
+            e = id_at<SMEM_IDS>(ids, p);
             ok = e >= 0 && e < E;
-            for (int q = 0; q < j && ok; ++q) ok = ld_dep(ids + (size_t)t * k + q) != e;
+            for (int q = 0; q < j && ok; ++q) ok = id_at<SMEM_IDS>(ids, (size_t)t * k + q) != e;
         }
         const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
         const int leader = __ffs(grp) - 1;
@@ -135,7 +153,7 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
     for (int p = warp * 32 + lane; p < P; p += SORT_THREADS) {
         const int r = o.pos[p];
         if (r >= 0) {
-            const int q = off[ld_dep(ids + p)] + r;
+            const int q = off[id_at<SMEM_IDS>(ids, p)] + r;
             o.pos[p] = q;
         }
     }
@@ -158,7 +176,7 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
     }
 }
 
-// The same outputs for P = S * k <= SORT_THREADS picks, by pairwise counting
+// The same outputs for P = S * k <= SMALL_SORT_PICKS picks, by pairwise counting
 // in one CTA (three barriers, no global round trip).  With key_p = (e_p, p)
 // over the valid picks, a pick's position is r_p = #{q : key_q < key_p} =
 // lt + eqb, where lt = #{q : e_q < e_p} is the start of expert e_p's segment
@@ -246,12 +264,21 @@ __device__ __forceinline__ void sort_picks_small(const int32_t* ids, int S, int 
     }
 }
 
+// moe_experts (ids from the caller): ids in global memory.
 __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* ids, int S, int E, int k,
                                                        SortOut o) {
     extern __shared__ int32_t smem[];
     pdl_wait();
     pdl_trigger();   // after the wait: see launch_gather
-    sort_picks(ids, S, E, k, o, smem);
+    const int P = S * k;
+    if (P <= SMALL_SORT_PICKS) {
+        int32_t* sids = smem + 2 * P;
+        for (int i = threadIdx.x; i < P; i += SORT_THREADS) sids[i] = ld_dep(ids + i);
+        __syncthreads();
+        sort_picks_small(sids, S, E, k, o, smem);
+    } else {
+        sort_picks<false>(ids, S, E, k, o, smem);
+    }
 }
 
 // moe_forward at small S: the sigmoid top-k of every token (one warp a token,
@@ -264,7 +291,8 @@ __global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* L,
                                                             float* __restrict__ weights, SortOut o) {
     extern __shared__ int32_t smem[];
     pdl_trigger();
-    int32_t* sids = smem + 2 * S * k;   // [S][k]
+    const int P = S * k;
+    int32_t* sids = smem + (P <= SMALL_SORT_PICKS ? 2 * P : sort_smem_ints(E));   // [S][k]
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     float b[MAXE];
     load_bias(bias, E, lane, b);   // an input of the call: read before the wait
@@ -273,7 +301,8 @@ __global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* L,
         topk_token(L + (size_t)t * E, b, E, k, lane, sids + (size_t)t * k, weights + (size_t)t * k);
     __syncthreads();
     for (int i = threadIdx.x; i < S * k; i += SORT_THREADS) ids[i] = sids[i];
-    sort_picks_small(sids, S, E, k, o, smem);
+    if (P <= SMALL_SORT_PICKS) sort_picks_small(sids, S, E, k, o, smem);
+    else sort_picks<true>(sids, S, E, k, o, smem);
 }
 
 // Token rows of the expert GEMMs.  grid (S * k), one pick p = t * k + j a
@@ -338,7 +367,7 @@ static cudaError_t launch_gather(const moe_shape& s, const WsLayout& L, const Pt
 }
 
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    const size_t smem = (size_t)sort_smem_ints(s.E) * sizeof(int32_t);
+    const size_t smem = (size_t)sort_smem_ints_for(s.E, s.S * s.k, false) * sizeof(int32_t);
     timing_begin(K_SORT, st);
     cudaError_t e = launch_pdl(k_sort, dim3(1), dim3(SORT_THREADS), smem, st, (const int32_t*)p.ids, s.S, s.E, s.k,
                                sort_out(L, p.ws));
@@ -354,7 +383,7 @@ bool topk_sort_fits(const moe_shape& s) {
 }
 
 cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    const size_t smem = (size_t)3 * s.S * s.k * sizeof(int32_t);   // ids, keys, tile starts
+    const size_t smem = (size_t)sort_smem_ints_for(s.E, s.S * s.k, true) * sizeof(int32_t);
     auto kern = s.E <= 256 ? k_topk_sort<256 / 32> : k_topk_sort<512 / 32>;
     cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
