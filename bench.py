@@ -355,6 +355,22 @@ def run_ours(args, cfg: mi.MoEConfig):
            "d2h_bytes_per_step": cfg.S * cfg.d * 4 + cfg.S * cfg.k * 8,
            "steps": E2, "api": "moe_forward_host (pinned host x in, ids/weights/out back)"}
 
+    # --- moe_experts alone (the route's ids and weights given) ----------------
+    E3 = min(K, 500)
+    ev3 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E3)]
+    for i in range(E3):
+        flush.zero_()
+        ev3[i][0].record(stream)
+        moe.experts(shape, blk.x, blk.ids, blk.weights, blk.w13, blk.w13s, blk.w2, blk.w2s, blk.norm_w,
+                    blk.out, blk.ws)
+        ev3[i][1].record(stream)
+    torch.cuda.synchronize(dev)
+    moe.check_device_status(blk.ws, "moe_experts steps")
+    ex_ms, ex_units = aggregate(dist, sum(a.elapsed_time(b) for a, b in ev3), E3 * cfg.S, dev)
+    experts_api = {"value": ex_units / (ex_ms / 1e3), "unit": "tokens/s", "ms_per_call": ex_ms / E3,
+                   "steps": E3, "api": "moe_experts (sort, gather, expert GEMMs, combine; ids and "
+                                       "weights from the route, device buffers)"}
+
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
         tps, ntok, el = oracle_tokens_per_s(inp, args.cpu_seconds, chunk=min(cfg.S, 8))
@@ -373,6 +389,7 @@ def run_ours(args, cfg: mi.MoEConfig):
             "kernels_ms": kmean,
             "cpu_baseline": cpu,
             "e2e": e2e,
+            "moe_experts": experts_api,
             "gpu_launches": launches_per_step * K,
             "launches_per_step": launches_per_step,
             "clocks": clk,
