@@ -79,6 +79,10 @@ SMALL = [
     mi.MoEConfig("s33", S=33, d=512, E=12, k=3, I=384, zipf=1.1),
     mi.MoEConfig("kE", S=5, d=128, E=4, k=4, I=128),
     mi.MoEConfig("s70", S=70, d=256, E=8, k=2, I=256),      # > NT picks per expert
+    mi.MoEConfig("s160", S=160, d=256, E=8, k=2, I=128),    # 32-pick tiles (40 picks per expert)
+    mi.MoEConfig("maxEk", S=4, d=256, E=512, k=16, I=128),  # E and k at their maxima
+    mi.MoEConfig("maxd", S=2, d=16384, E=8, k=2, I=128),    # d at its maximum (two gather passes)
+    mi.MoEConfig("maxI", S=2, d=256, E=4, k=1, I=8192),     # I at its maximum
 ]
 
 
