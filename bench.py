@@ -168,13 +168,21 @@ KERNEL_SOURCES = {
 }
 
 
+def _code_only(text: str) -> str:
+    """C++/CUDA source without comments and layout: what a profile describes."""
+    text = re.sub(r"/\*.*?\*/", " ", text, flags=re.S)
+    text = re.sub(r"//[^\n]*", " ", text)
+    return " ".join(text.split())
+
+
 def kernel_source_sha(name: str) -> str:
+    """Hash of the code (comments and whitespace removed) of a kernel's sources."""
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "mxfp4_mixture_experts_route_gb300", "csrc")
     files = KERNEL_SOURCES.get(name)
     paths = [os.path.join(csrc, f) for f in files] if files else sorted(glob.glob(os.path.join(csrc, "*")))
     for p in paths:
-        h.update(open(p, "rb").read())
+        h.update(_code_only(open(p, encoding="utf-8").read()).encode())
     return h.hexdigest()[:12]
 
 

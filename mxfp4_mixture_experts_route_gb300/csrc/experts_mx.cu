@@ -79,7 +79,7 @@ constexpr int A_TX = AROWS * KS / 2;         // packed bytes of a weight tile: t
 #ifndef MOE_MX_WIDE_TOKEN_STAGES
 #define MOE_MX_WIDE_TOKEN_STAGES 3
 #endif
-constexpr int NSB_DEF = MOE_MX_TOKEN_STAGES; // token-tile stages (two for 64-pick tiles)
+constexpr int NSB_DEF = MOE_MX_TOKEN_STAGES; // token-tile stages (MOE_MX_WIDE_TOKEN_STAGES for 64-pick tiles)
 constexpr int TMEM_COLS = 512;
 constexpr int NMMA_MAX = 2;                  // MMA-issuing warps (one thread each; one for 64-pick tiles)
 // One stage's scale slot in TMEM, 64 columns: the weight scales of K steps
