@@ -251,16 +251,18 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate, const
 }  // extern "C"
 
 namespace {
-// The device address of a pinned host buffer the GPU reads and writes in place
-// (cudaHostAlloc'd or registered memory under unified addressing; on GB300 over
-// the coherent CPU-GPU link), else nullptr: pageable memory is staged.
+// The device address of a 16-byte aligned pinned host buffer the GPU reads and
+// writes in place (cudaHostAlloc'd or registered memory under unified
+// addressing; on GB300 over the coherent CPU-GPU link), else nullptr: pageable
+// or unaligned memory is staged.
 void* device_view(const void* host) {
     cudaPointerAttributes at;
     if (cudaPointerGetAttributes(&at, host) != cudaSuccess) {
         cudaGetLastError();
         return nullptr;
     }
-    return at.type == cudaMemoryTypeHost ? at.devicePointer : nullptr;
+    if (at.type != cudaMemoryTypeHost || at.devicePointer == nullptr) return nullptr;
+    return ((uintptr_t)at.devicePointer & 15) == 0 ? at.devicePointer : nullptr;
 }
 }  // namespace
 
@@ -306,7 +308,6 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
         rc = cuda_rc(cudaMemcpyAsync(x_dev, x_host, (size_t)shape->S * shape->d * 2, cudaMemcpyHostToDevice, st));
         if (rc) return rc;
     }
-    if (!a16(x_dev) || !a16(out_dev) || !a16(ids_dev) || !a16(wts_dev)) return MOE_ERR_ALIGNMENT;
     rc = moe_forward(shape, x_dev, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids_dev, wts_dev,
                      out_dev, ws, ws_bytes, stream);
     if (rc) return rc;
