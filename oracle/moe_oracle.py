@@ -157,7 +157,10 @@ def score_gap(L32: np.ndarray, bias: np.ndarray, k: int) -> np.ndarray:
 
 
 def silu(g: np.ndarray) -> np.ndarray:
-    return g / (1.0 + np.exp(-g))
+    """SiLU(g) = g * sigmoid(g), with sigmoid(g) = (1 + tanh(g / 2)) / 2: the
+    same function, written so that no exponential overflows for large |g|."""
+    g = np.asarray(g, dtype=np.float64)
+    return g * 0.5 * (1.0 + np.tanh(0.5 * g))
 
 
 def expert_ffn(xf: np.ndarray, w13: np.ndarray, w13s: np.ndarray,
