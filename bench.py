@@ -52,6 +52,10 @@ def parse_args():
     ap.add_argument("--cpu-seconds", type=float, default=12.0,
                     help="budget of the CPU-oracle baseline sample")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-config", action="store_true",
+                    help="time only the --config workload, not the other verify/prefill workloads")
+    ap.add_argument("--experts", type=int, default=None,
+                    help="override E (smaller device footprint for ncu captures; not a bench line)")
     return ap.parse_args()
 
 
@@ -142,12 +146,39 @@ class ClockSampler:
 # ---------------------------------------------------------------------------
 # roofline helpers
 # ---------------------------------------------------------------------------
+FALLBACK_BF16_TFLOPS = 1900.0
+FALLBACK_BF16_TFLOPS_SUSTAINED = 1700.0
+
+
 def measured_peaks():
     if os.path.exists(PEAKS_FILE):
         with open(PEAKS_FILE) as f:
             p = json.load(f)
         return float(p["hbm_gbs"]), "measured"
     return FALLBACK_HBM_GBS, "fallback"
+
+
+def measured_tensor_peaks():
+    """(bf16 burst TFLOP/s, bf16 sustained TFLOP/s, source)."""
+    if os.path.exists(PEAKS_FILE):
+        with open(PEAKS_FILE) as f:
+            p = json.load(f)
+        if "bf16_tflops" in p:
+            return (float(p["bf16_tflops"]), float(p.get("bf16_tflops_sustained", p["bf16_tflops"])),
+                    "measured")
+    return FALLBACK_BF16_TFLOPS, FALLBACK_BF16_TFLOPS_SUSTAINED, "fallback"
+
+
+# configurations whose expert GEMMs are bound by the tensor pipe, not HBM
+TENSOR_BOUND = {"prefill_s4096_zipf"}
+
+
+def algorithmic_flops(cfg: mi.MoEConfig) -> dict:
+    """Per launch: the flops the block must do at least -- 2 flops a multiply-add
+    over the three expert matrices of every pick (S k 6 I d) and the router
+    (2 S E d)."""
+    experts = cfg.S * cfg.k * 6 * cfg.I * cfg.d
+    return {"experts": experts, "step": experts + 2 * cfg.S * cfg.E * cfg.d}
 
 
 def algorithmic_bytes(cfg: mi.MoEConfig, n_touched: int) -> dict:
@@ -186,10 +217,10 @@ def kernel_source_sha(name: str) -> str:
     return h.hexdigest()[:12]
 
 
-def profiled_traffic(kernel: str, workload: str):
+def profiled_traffic(kernel: str, workload: str, profiles_dir: str | None = None):
     """DRAM bytes per launch from a committed ncu summary of this kernel and
     workload, if the library sources have not changed since it was taken."""
-    path = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    path = os.path.join(profiles_dir or os.path.join(ROOT, "profiles"), f"{kernel}_{workload}.md")
     if not os.path.exists(path):
         return None
     txt = open(path).read()
@@ -227,6 +258,9 @@ def run_reference(args, cfg: mi.MoEConfig):
         return
     import oracle as O
     inp = mi.make_inputs(cfg)
+    # the touched experts of the whole workload, as the GPU arm's config reports them
+    rids, _ = O.route(O.router_logits(inp.x, inp.w_gate, inp.logit_off), inp.bias, cfg.k)
+    n_touched = int(len(np.unique(rids)))
     chunk = 1
     for _ in range(args.warmup):
         O.moe_forward(inp, np.arange(chunk))
@@ -240,7 +274,7 @@ def run_reference(args, cfg: mi.MoEConfig):
         "impl": "reference", "metric": METRIC, "value": val, "unit": "tokens/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * el / args.steps,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
-        "data": "synthetic", "config": workload_config(cfg, None),
+        "data": "synthetic", "config": workload_config(cfg, n_touched),
         "cpu_baseline": {"value": val, "unit": "tokens/s", "cores": oracle_threads(), "kind": "oracle",
                          "sample": f"1 token row a step (token s mod {cfg.S}), numpy fp64 oracle"},
         "e2e": {"value": val, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -260,6 +294,120 @@ def workload_config(cfg: mi.MoEConfig, n_touched):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+def timed_steps(fn, n, flush, stream, warmup=0):
+    """Per-step device milliseconds of fn() over n steps (CUDA events on the
+    launch stream), the L2 flushed before every step outside the events."""
+    import torch
+    for _ in range(warmup):
+        flush.zero_()
+        fn()
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(n)]
+    for i in range(n):
+        flush.zero_()
+        ev[i][0].record(stream)
+        fn()
+        ev[i][1].record(stream)
+    torch.cuda.synchronize()
+    return [x.elapsed_time(y) for x, y in ev]
+
+
+def kernel_times(moe, fn, n, flush):
+    """Mean device milliseconds of each of the library's kernels over n steps
+    (the library's per-launch event timer), their totals and launches a step."""
+    import torch
+    moe.timing_enable(64 * n)
+    for _ in range(n):
+        flush.zero_()
+        fn()
+    torch.cuda.synchronize()
+    recs = moe.timing_collect(64 * n)
+    moe.timing_enable(0)
+    per = {}
+    for name, ms in recs:
+        per.setdefault(name, []).append(ms)
+    return {k: statistics.fmean(v) for k, v in per.items()}, {k: sum(v) for k, v in per.items()}, len(recs) // n
+
+
+def roofline(cfg: mi.MoEConfig, n_touched: int, kmean: dict, ktot: dict, workload: str):
+    """The dominant kernel's roofline: HBM bytes (weight streaming) or, for the
+    tensor-bound prefill workload, flops against the measured bf16 peak."""
+    dom = max(ktot, key=ktot.get)
+    share = ktot[dom] / sum(ktot.values())
+    if cfg.name in TENSOR_BOUND and dom == "experts":
+        burst, sust, src = measured_tensor_peaks()
+        fl = algorithmic_flops(cfg)["experts"]
+        ach = fl / (kmean[dom] * 1e-3) / 1e12
+        return {"kernel": dom, "bound": "tensor", "achieved": ach, "peak": burst, "unit": "TFLOP/s",
+                "frac": ach / burst, "frac_of_sustained": ach / sust,
+                "peak_source": f"{src} bf16 dense (MEASURED_PEAKS.json bf16_tflops; sustained "
+                               f"{sust}); the MMA runs block-scaled e2m1 x e4m3 on hi and lo token rows",
+                "traffic": profiled_traffic(dom, workload), "algorithmic_flops_per_launch": fl,
+                "mean_launch_ms": kmean[dom], "share_of_step": share}
+    hbm_peak, peak_src = measured_peaks()
+    alg = algorithmic_bytes(cfg, n_touched)
+    nb = alg.get(dom)
+    if nb is None:
+        return None
+    ach = nb / (kmean[dom] * 1e-3) / 1e9
+    return {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
+            "frac": ach / hbm_peak, "frac_of_8tbs": ach / 8000.0,
+            "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)" if peak_src == "measured"
+            else "fallback 6.8 TB/s",
+            "traffic": profiled_traffic(dom, workload), "algorithmic_bytes_per_launch": nb,
+            "mean_launch_ms": kmean[dom], "share_of_step": share}
+
+
+def upload(moe, cfg: mi.MoEConfig, inp: mi.MoEInputs, dev, share=None):
+    """Device copies of a workload's tensors; weights shared with `share` (an
+    earlier block of the same d, E, I, seed) instead of uploaded again."""
+    shape = moe.MoEShape.of(cfg.S, cfg.d, cfg.E, cfg.k, cfg.I, post_norm=cfg.post_norm,
+                            logit_offset=bool(cfg.zipf), norm_eps=cfg.norm_eps)
+    if share is not None:
+        return moe.DeviceWeights(shape, inp.x, share.w_gate, share.bias, inp.logit_off, share.w13, share.w13s,
+                                 share.w2, share.w2s, inp.norm_w, device=dev)
+    return moe.DeviceWeights(shape, inp.x, inp.w_gate, inp.bias, inp.logit_off, inp.w13, inp.w13s,
+                             inp.w2, inp.w2s, inp.norm_w, device=dev)
+
+
+def workload_inputs(cfg: mi.MoEConfig, weights_from: mi.MoEInputs | None = None) -> mi.MoEInputs:
+    """Seeded inputs; the weights of an earlier workload with the same d, E, I
+    (the same streams) are reused instead of drawn again."""
+    if weights_from is None:
+        return mi.make_inputs(cfg)
+    att = mi.stored_attempts(cfg)
+    w = weights_from
+    return mi.MoEInputs(cfg=cfg, seed=0, x=mi.gen_x(cfg, 0, att), w_gate=w.w_gate, bias=w.bias,
+                        logit_off=mi.gen_logit_offset(cfg), w13=w.w13, w13s=w.w13s, w2=w.w2, w2s=w.w2s,
+                        norm_w=mi.gen_norm_w(cfg), attempts=att if att is not None else np.zeros(cfg.S, np.int64))
+
+
+# per-config entries of the default run: steps timed (the workloads' step
+# times run from ~0.15 to ~4 ms)
+PER_CONFIG_STEPS = {2: 300, 3: 100, 4: 30}
+
+
+def per_config_entry(moe, blk, cfg, flush, stream, steps):
+    ms = timed_steps(blk.forward, steps, flush, stream, warmup=3)
+    moe.check_device_status(blk.ws, f"{cfg.name} steps")
+    n_touched = int(len(np.unique(blk.ids.cpu().numpy())))
+    kmean, ktot, lps = kernel_times(moe, blk.forward, max(3, steps // 5), flush)
+    step = statistics.fmean(ms)
+    alg = algorithmic_bytes(cfg, n_touched)
+    e = {"workload": cfg.name, "S": cfg.S, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I,
+         "n_touched": n_touched, "steps": steps, "ms_per_step": step,
+         "ms_per_step_median": statistics.median(ms), "tokens_per_s": cfg.S / (step * 1e-3),
+         "step_gbs": alg["step"] / (step * 1e-3) / 1e9, "launches_per_step": lps,
+         "kernels_ms": kmean, "roofline": roofline(cfg, n_touched, kmean, ktot, cfg.name)}
+    if cfg.name in TENSOR_BOUND:
+        burst, sust, _ = measured_tensor_peaks()
+        tf = algorithmic_flops(cfg)["step"] / (step * 1e-3) / 1e12
+        e.update({"step_tflops": tf, "step_frac_of_bf16": tf / burst, "step_frac_of_bf16_sustained": tf / sust})
+    else:
+        hbm, _ = measured_peaks()
+        e["step_frac_of_hbm"] = e["step_gbs"] / hbm
+    return e
+
+
 def run_ours(args, cfg: mi.MoEConfig):
     import torch
     import mxfp4_mixture_experts_route_gb300 as moe
@@ -270,10 +418,8 @@ def run_ours(args, cfg: mi.MoEConfig):
     dev = torch.device("cuda", local)
 
     inp = mi.make_inputs(cfg)
-    shape = moe.MoEShape.of(cfg.S, cfg.d, cfg.E, cfg.k, cfg.I, post_norm=cfg.post_norm,
-                            logit_offset=bool(cfg.zipf), norm_eps=cfg.norm_eps)
-    blk = moe.DeviceWeights(shape, inp.x, inp.w_gate, inp.bias, inp.logit_off, inp.w13, inp.w13s,
-                            inp.w2, inp.w2s, inp.norm_w, device=dev)
+    blk = upload(moe, cfg, inp, dev)
+    shape = blk.shape
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
     flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
     stream = torch.cuda.current_stream(dev)
@@ -311,34 +457,9 @@ def run_ours(args, cfg: mi.MoEConfig):
     value = units / (ms_total / 1e3)
 
     # --- per-kernel timing pass (roofline) ----------------------------------
-    T = max(1, args.timing_steps)
-    launches_per_step = None
-    moe.timing_enable(64 * T)
-    for _ in range(T):
-        flush.zero_()
-        blk.forward()
-    torch.cuda.synchronize(dev)
-    recs = moe.timing_collect(64 * T)
-    moe.timing_enable(0)
-    launches_per_step = len(recs) // T
-    per_kernel = {}
-    for name, ms in recs:
-        per_kernel.setdefault(name, []).append(ms)
-    kmean = {k: statistics.fmean(v) for k, v in per_kernel.items()}
-    ktot = sum(sum(v) for v in per_kernel.values())
-    dom = max(kmean, key=lambda k: sum(per_kernel[k]))
-    hbm_peak, peak_src = measured_peaks()
+    kmean, ktot, launches_per_step = kernel_times(moe, blk.forward, max(1, args.timing_steps), flush)
+    roof = roofline(cfg, n_touched, kmean, ktot, cfg.name)
     alg = algorithmic_bytes(cfg, n_touched)
-    dom_bytes = alg.get(dom)
-    roof = None
-    if dom_bytes is not None:
-        ach = dom_bytes / (kmean[dom] * 1e-3) / 1e9
-        roof = {"kernel": dom, "bound": "hbm", "achieved": ach, "peak": hbm_peak, "unit": "GB/s",
-                "frac": ach / hbm_peak, "peak_source": f"{peak_src} (MEASURED_PEAKS.json hbm_gbs)"
-                if peak_src == "measured" else "fallback 6.8 TB/s",
-                "traffic": profiled_traffic(dom, cfg.name),
-                "algorithmic_bytes_per_launch": dom_bytes, "mean_launch_ms": kmean[dom],
-                "share_of_step": sum(per_kernel[dom]) / ktot}
     step_mean_ms = ms_total / K
     step_gbs = alg["step"] / (statistics.fmean(step_ms) * 1e-3) / 1e9
 
@@ -347,37 +468,55 @@ def run_ours(args, cfg: mi.MoEConfig):
     oh = torch.empty((cfg.S, cfg.d), dtype=torch.float32).pin_memory()
     ih = torch.empty((cfg.S, cfg.k), dtype=torch.int32).pin_memory()
     wh = torch.empty((cfg.S, cfg.k), dtype=torch.float32).pin_memory()
-    E2 = min(K, 500)
-    ev2 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E2)]
-    for i in range(E2):
-        flush.zero_()
-        ev2[i][0].record(stream)
+
+    def e2e_step():
         moe.forward_host(shape, xh, blk.w_gate, blk.bias, blk.logit_off, blk.w13, blk.w13s, blk.w2,
                          blk.w2s, blk.norm_w, ih, wh, oh, blk.ws)
-        ev2[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+
+    E2 = min(K, 500)
+    e2e_ms = timed_steps(e2e_step, E2, flush, stream, warmup=max(3, args.warmup))
     moe.check_device_status(blk.ws, "e2e steps")
-    e2e_ms, e2e_units = aggregate(dist, sum(a.elapsed_time(b) for a, b in ev2), E2 * cfg.S, dev)
-    e2e = {"value": e2e_units / (e2e_ms / 1e3), "unit": "tokens/s",
+    e2e_tot, e2e_units = aggregate(dist, sum(e2e_ms), E2 * cfg.S, dev)
+    e2e = {"value": e2e_units / (e2e_tot / 1e3), "unit": "tokens/s",
+           "median_value": cfg.S / (statistics.median(e2e_ms) * 1e-3),
            "h2d_bytes_per_step": cfg.S * cfg.d * 2,
            "d2h_bytes_per_step": cfg.S * cfg.d * 4 + cfg.S * cfg.k * 8,
-           "steps": E2, "api": "moe_forward_host (pinned host x in, ids/weights/out back)"}
+           "steps": E2, "warmup": max(3, args.warmup),
+           "api": "moe_forward_host (pinned host x in, ids/weights/out back)"}
 
     # --- moe_experts alone (the route's ids and weights given) ----------------
-    E3 = min(K, 500)
-    ev3 = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(E3)]
-    for i in range(E3):
-        flush.zero_()
-        ev3[i][0].record(stream)
+    def experts_step():
         moe.experts(shape, blk.x, blk.ids, blk.weights, blk.w13, blk.w13s, blk.w2, blk.w2s, blk.norm_w,
                     blk.out, blk.ws)
-        ev3[i][1].record(stream)
-    torch.cuda.synchronize(dev)
+
+    blk.forward()
+    E3 = min(K, 500)
+    ex_ms = timed_steps(experts_step, E3, flush, stream, warmup=max(3, args.warmup))
     moe.check_device_status(blk.ws, "moe_experts steps")
-    ex_ms, ex_units = aggregate(dist, sum(a.elapsed_time(b) for a, b in ev3), E3 * cfg.S, dev)
-    experts_api = {"value": ex_units / (ex_ms / 1e3), "unit": "tokens/s", "ms_per_call": ex_ms / E3,
-                   "steps": E3, "api": "moe_experts (sort, gather, expert GEMMs, combine; ids and "
-                                       "weights from the route, device buffers)"}
+    ex_tot, ex_units = aggregate(dist, sum(ex_ms), E3 * cfg.S, dev)
+    experts_api = {"value": ex_units / (ex_tot / 1e3), "unit": "tokens/s", "ms_per_call": ex_tot / E3,
+                   "ms_per_call_median": statistics.median(ex_ms), "steps": E3,
+                   "api": "moe_experts (sort, gather, expert GEMMs, combine; ids and "
+                          "weights from the route, device buffers)"}
+
+    # --- the other workloads (rank 0 of a replica run only) -------------------
+    per_config = None
+    if rank == 0 and not args.no_per_config:
+        per_config = {}
+        prev_inp, prev_blk = inp, blk
+        for ci in sorted(PER_CONFIG_STEPS):
+            c = mi.CONFIGS[ci]
+            if c.name == cfg.name:
+                continue
+            same_w = (prev_inp.cfg.d, prev_inp.cfg.E, prev_inp.cfg.I) == (c.d, c.E, c.I)
+            if not same_w:
+                del prev_blk
+                torch.cuda.empty_cache()
+            ci_inp = workload_inputs(c, prev_inp if same_w else None)
+            ci_blk = upload(moe, c, ci_inp, dev, share=prev_blk if same_w else None)
+            per_config[c.name] = per_config_entry(moe, ci_blk, c, flush, stream, PER_CONFIG_STEPS[ci])
+            prev_inp, prev_blk = ci_inp, ci_blk
+        del prev_blk
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:
@@ -389,7 +528,8 @@ def run_ours(args, cfg: mi.MoEConfig):
     if rank == 0:
         line = {
             "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": ws_n, "steps": K,
-            "warmup": args.warmup, "ms_per_step": step_mean_ms, "higher_is_better": True,
+            "warmup": args.warmup, "ms_per_step": step_mean_ms,
+            "ms_per_step_median": statistics.median(step_ms), "higher_is_better": True,
             "scaling": "weak", "vs_baseline": None, "dtype": DTYPE, "data": "synthetic",
             "config": workload_config(cfg, n_touched),
             "achieved_hbm_gbs_step": step_gbs,
@@ -398,6 +538,7 @@ def run_ours(args, cfg: mi.MoEConfig):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "moe_experts": experts_api,
+            "per_config": per_config,
             "gpu_launches": launches_per_step * K,
             "launches_per_step": launches_per_step,
             "clocks": clk,
@@ -417,6 +558,9 @@ DTYPE = "e2m1xe4m3"
 def main():
     args = parse_args()
     cfg = mi.CONFIGS[args.config]
+    if args.experts is not None:
+        cfg = cfg.with_(E=args.experts, name=f"{cfg.name}_E{args.experts}")
+        args.no_per_config = True
     if args.impl == "reference":
         run_reference(args, cfg)
     else:

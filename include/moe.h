@@ -209,12 +209,17 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
  * no counterpart: their launchers always receive a scratch buffer.
  *
  * Scratch comes from a 32 MiB static device array inside the library, which
- * every GPU that loads the library holds until the process exits.  Shapes
- * whose moe_workspace_bytes() exceeds 32 MiB are rejected with
- * MOE_ERR_WORKSPACE before anything is enqueued (S * k <= 256 at d = 4096,
- * I = 1024, E = 256 fits).  No call allocates or frees memory.  The first call
- * on a device looks up the array's device address once (cudaGetSymbolAddress,
- * with that device current); make that first call before any stream capture.
+ * every GPU that uses this entry point holds until the process exits.  The
+ * library's device modules load lazily (CUDA's default), so the 32 MiB are
+ * reserved by the first call on a device, which loads the array's module and
+ * looks up its device address once (cudaGetSymbolAddress, with that device
+ * current).  Make that first call as a warm-up: before a memory pool claims
+ * the whole GPU (else it fails with MOE_ERR_CUDA, reported on stderr) and
+ * before any stream capture.  No call allocates or frees memory itself.
+ * Shapes whose moe_workspace_bytes() exceeds 32 MiB are rejected with
+ * MOE_ERR_WORKSPACE (S * k <= 256 at d = 4096, I = 1024, E = 256 fits), and
+ * every argument check of moe_forward runs, with the same codes, before the
+ * array is touched: a rejected call enqueues nothing.
  *
  * Every call on a device shares the one array, which keeps the previous
  * call's contents; each call clears its status block first.  Calls that
@@ -241,6 +246,34 @@ int moe_forward_noalloc(const moe_shape* shape, const void* x, const void* w_gat
  * the wait that ran out.
  */
 int moe_device_status(void* ws, int32_t* detail, void* stream);
+
+/*
+ * Workspace regions (diagnostics, pure host function): byte offset and size
+ * of one region of the workspace of `shape`, for reading intermediate results
+ * back after a call (tests and profiling).  Returns MOE_OK, or
+ * MOE_ERR_INVALID_ARG / MOE_ERR_UNSUPPORTED_SHAPE.  P = S * k picks; a pick's
+ * sorted position r groups the picks by ascending expert id (k3 page,
+ * dn_loads: tasks over a table of the experts that have picks).
+ *   MOE_WS_STATUS  int32 [64]: status, detail, valid picks, work tiles, ...
+ *   MOE_WS_POS     int32 [P]: sorted position r of pick t*k + j (-1: invalid)
+ *   MOE_WS_TILES   int32 [max tiles][4]: expert, first position, picks, 0;
+ *                  the first "work tiles" entries are this call's tiles
+ *   MOE_WS_XQ      uint8 [2P][d]: e4m3 rows 2r (hi) and 2r + 1 (lo) of the
+ *                  token of the pick at position r
+ *   MOE_WS_XS      uint8 [ceil(d/256)][P + 64][16]: e8m0 scale of 32-element
+ *                  block b of position r at [b / 8][r][b % 8]
+ *   MOE_WS_HQ, MOE_WS_HS  the same for h = silu(g) * u (K = I)
+ *   MOE_WS_Y       fp32 [P][d]: expert output of the pick at position r
+ */
+#define MOE_WS_STATUS 0
+#define MOE_WS_POS    1
+#define MOE_WS_TILES  2
+#define MOE_WS_XQ     3
+#define MOE_WS_XS     4
+#define MOE_WS_HQ     5
+#define MOE_WS_HS     6
+#define MOE_WS_Y      7
+int moe_workspace_region(const moe_shape* shape, int region, size_t* offset, size_t* bytes);
 
 /*
  * Per-kernel timing (diagnostics, host side).  After moe_timing_enable(n) with

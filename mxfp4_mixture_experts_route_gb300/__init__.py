@@ -31,7 +31,11 @@ MOE_LOGIT_OFFSET = 2
 # every symbol include/moe.h declares
 EXPORTS = ("moe_abi_version", "moe_strerror", "moe_workspace_bytes", "moe_workspace_init",
            "moe_route", "moe_experts", "moe_forward", "moe_forward_host", "moe_device_status",
-           "moe_timing_enable", "moe_timing_collect", "moe_kernel_name", "moe_forward_noalloc")
+           "moe_timing_enable", "moe_timing_collect", "moe_kernel_name", "moe_forward_noalloc",
+           "moe_workspace_region")
+
+# workspace regions (moe_workspace_region)
+MOE_WS_STATUS, MOE_WS_POS, MOE_WS_TILES, MOE_WS_XQ, MOE_WS_XS, MOE_WS_HQ, MOE_WS_HS, MOE_WS_Y = range(8)
 
 
 class MoEShape(ctypes.Structure):
@@ -68,27 +72,34 @@ def lib() -> ctypes.CDLL:
         if not os.path.exists(LIB_PATH):
             raise RuntimeError(f"libmoe.so not built ({LIB_PATH}); run "
                                "`python -c 'import __graft_entry__ as g; g.build()'`")
-        L = ctypes.CDLL(LIB_PATH)
-        L.moe_abi_version.restype = ctypes.c_int
-        L.moe_strerror.restype = ctypes.c_char_p
-        L.moe_strerror.argtypes = [ctypes.c_int]
-        L.moe_workspace_bytes.argtypes = [_SP, ctypes.POINTER(ctypes.c_size_t)]
-        L.moe_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
-        L.moe_route.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
-        L.moe_experts.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
-        L.moe_forward.argtypes = [_SP] + [_P] * 13 + [ctypes.c_size_t, _P]
-        L.moe_forward_host.argtypes = [_SP] + [_P] * 13 + [ctypes.c_size_t, _P]
-        L.moe_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
-        L.moe_forward_noalloc.argtypes = [_SP] + [_P] * 14
-        L.moe_timing_enable.argtypes = [ctypes.c_int]
-        L.moe_timing_collect.argtypes = [_P, _P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
-        L.moe_kernel_name.argtypes = [ctypes.c_int]
-        L.moe_kernel_name.restype = ctypes.c_char_p
-        for name in EXPORTS:
-            if name not in ("moe_strerror", "moe_kernel_name"):
-                getattr(L, name).restype = ctypes.c_int
-        _lib = L
+        _lib = load_library(LIB_PATH)
     return _lib
+
+
+def load_library(path: str) -> ctypes.CDLL:
+    """A build of the library at `path` with the entry points' C types set."""
+    L = ctypes.CDLL(path)
+    L.moe_abi_version.restype = ctypes.c_int
+    L.moe_strerror.restype = ctypes.c_char_p
+    L.moe_strerror.argtypes = [ctypes.c_int]
+    L.moe_workspace_bytes.argtypes = [_SP, ctypes.POINTER(ctypes.c_size_t)]
+    L.moe_workspace_init.argtypes = [_P, ctypes.c_size_t, _P]
+    L.moe_route.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.moe_experts.argtypes = [_SP, _P, _P, _P, _P, _P, _P, _P, _P, _P, _P, ctypes.c_size_t, _P]
+    L.moe_forward.argtypes = [_SP] + [_P] * 13 + [ctypes.c_size_t, _P]
+    L.moe_forward_host.argtypes = [_SP] + [_P] * 13 + [ctypes.c_size_t, _P]
+    L.moe_device_status.argtypes = [_P, ctypes.POINTER(ctypes.c_int32), _P]
+    L.moe_forward_noalloc.argtypes = [_SP] + [_P] * 14
+    L.moe_workspace_region.argtypes = [_SP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t),
+                                       ctypes.POINTER(ctypes.c_size_t)]
+    L.moe_timing_enable.argtypes = [ctypes.c_int]
+    L.moe_timing_collect.argtypes = [_P, _P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
+    L.moe_kernel_name.argtypes = [ctypes.c_int]
+    L.moe_kernel_name.restype = ctypes.c_char_p
+    for name in EXPORTS:
+        if name not in ("moe_strerror", "moe_kernel_name"):
+            getattr(L, name).restype = ctypes.c_int
+    return L
 
 
 def strerror(code: int) -> str:
@@ -121,6 +132,22 @@ def workspace_bytes(shape: MoEShape) -> int:
     n = ctypes.c_size_t(0)
     _check(lib().moe_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)), "moe_workspace_bytes")
     return n.value
+
+
+def workspace_region(shape: MoEShape, region: int) -> tuple[int, int]:
+    """(byte offset, bytes) of one workspace region (MOE_WS_*)."""
+    off, n = ctypes.c_size_t(0), ctypes.c_size_t(0)
+    _check(lib().moe_workspace_region(ctypes.byref(shape), region, ctypes.byref(off), ctypes.byref(n)),
+           "moe_workspace_region")
+    return off.value, n.value
+
+
+def read_region(shape: MoEShape, ws, region: int, dtype=None):
+    """A CPU copy of one workspace region (after the stream has finished): a
+    uint8 tensor, viewed as `dtype` when given."""
+    off, n = workspace_region(shape, region)
+    t = ws[off:off + n].cpu()
+    return t if dtype is None else t.view(dtype)
 
 
 def new_workspace(shape: MoEShape, device="cuda", stream=None):

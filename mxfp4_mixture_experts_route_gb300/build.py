@@ -40,27 +40,43 @@ def _run(cmd: list[str]) -> None:
         sys.stderr.write(r.stdout)
 
 
-def build_library(extra_flags: list[str] | None = None, verbose: bool = False) -> str:
-    """Compile csrc/*.cu and link libmoe.so; returns the library path."""
+def build_library(extra_flags: list[str] | None = None, verbose: bool = False, lib_path: str = LIB,
+                  build_dir: str = BUILD) -> str:
+    """Compile csrc/*.cu and link a library (libmoe.so unless lib_path says
+    otherwise; a variant with other flags takes its own build_dir); returns
+    the library path."""
     nvcc = _nvcc()
-    os.makedirs(BUILD, exist_ok=True)
-    os.makedirs(LIBDIR, exist_ok=True)
+    os.makedirs(build_dir, exist_ok=True)
+    os.makedirs(os.path.dirname(lib_path), exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")))
     flags = NVFLAGS + (extra_flags or [])
     if verbose:
         flags = flags + ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(BUILD, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(build_dir, os.path.basename(src)[:-3] + ".o")
         _run([nvcc, *ARCH, *flags, "-c", src, "-o", obj])
         return obj
 
     with ThreadPoolExecutor(max_workers=min(len(srcs), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(compile_one, srcs))
-    tmp = LIB + ".tmp"
+    tmp = lib_path + ".tmp"
     _run([nvcc, *ARCH, "-shared", "-o", tmp, *objs, "-lcudart"])
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib_path)
+    return lib_path
+
+
+# A test-only variant: every bounded device wait of the expert kernel gives
+# up after 1 ms instead of 2 s, and moe_test_unreachable_wait(1) makes the
+# first down unit of the first tile wait for a readiness count that is never
+# reached, so that the wait runs out.  Never the library the benchmark or a
+# user loads.
+WAIT_TEST_LIB = os.path.join(LIBDIR, "libmoe_waittest.so")
+
+
+def build_wait_test_library() -> str:
+    return build_library(["-DMOE_WAIT_TEST"], lib_path=WAIT_TEST_LIB,
+                         build_dir=os.path.join(PKG, "_build_waittest"))
 
 
 if __name__ == "__main__":

@@ -94,7 +94,14 @@ constexpr int NUM_WARPS = 13;
 constexpr int LOOKAHEAD = 2;                 // units the scheduler publishes ahead of the weight producer
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 constexpr int UR = 32;                       // unit ring entries
+#ifndef MOE_WAIT_TEST
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
+#else
+// test-only build: waits give up after 1 ms, and one down unit can be made to
+// wait for a readiness count that is never reached
+constexpr uint64_t WAIT_NS = 1000000ull;
+int g_unreachable_wait = 0;
+#endif
 
 // STMA: the e8m0 bytes of the weights come by TMA, 16 bytes (512 K) of each
 // row per stage, when the scale rows are 16-byte aligned (K % 512 == 0);
@@ -149,6 +156,9 @@ struct Args {
     const uint8_t* xs;    // [ceil(d/256)][P + NT_MAX][16] e8m0 block scales of the gathered tokens
     int d, I, P;
     int max_tiles;
+#ifdef MOE_WAIT_TEST
+    int unreachable;      // the first down unit of tile 0 waits for one gate_up unit too many
+#endif
 };
 
 // A tile entry of the sort's table (an earlier kernel's output: read through L2)
@@ -434,7 +444,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint64_t t0 = ptx::globaltimer();
                     uint32_t it = 0;
                     ready = 1;
-                    while (ptx::ld_acquire_gpu(&a.tile_ready[U.tile]) < (uint32_t)mb1) {
+#ifndef MOE_WAIT_TEST
+                    const uint32_t target = (uint32_t)mb1;
+#else
+                    const uint32_t target = (uint32_t)mb1 + (a.unreachable && U.tile == 0 && U.mb == 0 ? 1u : 0u);
+#endif
+                    while (ptx::ld_acquire_gpu(&a.tile_ready[U.tile]) < target) {
                         __nanosleep(32);
                         if ((++it & 63u) == 0u && (*abort_flag || ptx::globaltimer() - t0 > WAIT_NS)) {
                             fail(2);
@@ -801,6 +816,9 @@ cudaError_t launch_mx(const moe_shape& s, const WsLayout& L, const Ptrs& p, cuda
     a.I = s.I;
     a.P = L.max_picks;
     a.max_tiles = L.max_tiles;
+#ifdef MOE_WAIT_TEST
+    a.unreachable = g_unreachable_wait;
+#endif
     return launch_pdl(k_experts_mx<STMA, NTT>, dim3(num_sms()), dim3(NUM_THREADS), C::SMEM, st, tm_w13, tm_w2, tm_xq, tm_hq,
                       tm_w13s, tm_w2s, a);
 }
@@ -864,3 +882,13 @@ cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p,
 }
 
 }  // namespace moe
+
+#ifdef MOE_WAIT_TEST
+// Test-only export of the wait-test build: on != 0 makes the next launches'
+// first down unit of tile 0 wait for a count no kernel reaches, so its bounded
+// wait runs out (MOE_ERR_TIMEOUT, detail 2) and the kernel takes its abort path.
+extern "C" int moe_test_unreachable_wait(int on) {
+    moe::g_unreachable_wait = on != 0;
+    return 0;
+}
+#endif

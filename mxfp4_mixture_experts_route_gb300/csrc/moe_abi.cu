@@ -128,6 +128,20 @@ static int run_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cud
     return cuda_rc(launch_combine(s, L, p, st));
 }
 
+// Every host-side check of moe_forward (shape, pointers, alignment, device),
+// without the workspace: moe_forward_noalloc runs them before it touches its
+// scratch array, so a rejected call enqueues nothing.
+int check_forward_args(const moe_shape* s, const void* x, const void* w_gate, const float* bias,
+                       const float* logit_off, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                       const uint8_t* w2s, const float* norm_w, const int32_t* ids, const float* w,
+                       const float* out) {
+    int rc = check_shape(s);
+    if (!rc) rc = check_route_args(s, x, w_gate, bias, logit_off, ids, w);
+    if (!rc) rc = check_expert_args(s, x, ids, w, w13, w13s, w2, w2s, norm_w, out);
+    if (!rc) rc = check_device();
+    return rc;
+}
+
 // The whole block.  At small S the top-k and the sort share one kernel (one
 // launch and one global round trip of the ids fewer).
 static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
@@ -171,6 +185,26 @@ int moe_workspace_bytes(const moe_shape* shape, size_t* bytes) {
     if (rc) return rc;
     if (!bytes) return MOE_ERR_INVALID_ARG;
     *bytes = ws_layout(*shape).total;
+    return MOE_OK;
+}
+
+int moe_workspace_region(const moe_shape* shape, int region, size_t* offset, size_t* bytes) {
+    int rc = check_shape(shape);
+    if (rc) return rc;
+    if (!offset || !bytes) return MOE_ERR_INVALID_ARG;
+    const WsLayout L = ws_layout(*shape);
+    const size_t P = (size_t)shape->S * shape->k, rows = P + NT_MAX;
+    switch (region) {
+        case MOE_WS_STATUS: *offset = L.status; *bytes = sizeof(StatusBlock); break;
+        case MOE_WS_POS: *offset = L.pos; *bytes = P * 4; break;
+        case MOE_WS_TILES: *offset = L.tiles; *bytes = (size_t)L.max_tiles * sizeof(Tile); break;
+        case MOE_WS_XQ: *offset = L.xq; *bytes = 2 * P * shape->d; break;
+        case MOE_WS_XS: *offset = L.xs; *bytes = (size_t)((shape->d + 255) / 256) * rows * TOKEN_SCALE_ROW; break;
+        case MOE_WS_HQ: *offset = L.hq; *bytes = 2 * P * shape->I; break;
+        case MOE_WS_HS: *offset = L.hs; *bytes = (size_t)((shape->I + 255) / 256) * rows * TOKEN_SCALE_ROW; break;
+        case MOE_WS_Y: *offset = L.y; *bytes = P * shape->d * 4; break;
+        default: return MOE_ERR_INVALID_ARG;
+    }
     return MOE_OK;
 }
 

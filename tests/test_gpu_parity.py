@@ -49,27 +49,138 @@ def test_configs_full(ci):
     _check(inp, ids, w, out)
 
 
-def test_config3_sampled():
-    cfg = mi.CONFIGS[3]
+def _tile_picks(cfg):
+    """Picks per tile, as the library chooses it from the average picks per
+    expert (8 up to 2, 16 below 32, 32 below 64, else 64)."""
+    P = cfg.S * cfg.k
+    if P <= 2 * cfg.E:
+        return 8
+    if P >= 64 * cfg.E:
+        return 64
+    return 32 if P >= 32 * cfg.E else 16
+
+
+def _sort_state(blk, ids):
+    """The GPU's expert sort of the last call, read back from the workspace, and
+    checked for what is unique about it: every expert's picks fill one segment
+    of positions (experts in ascending order), cut into tiles of nt picks (the
+    last one partial).  The order of picks inside a segment is not unique.
+    Returns (slot [S, k], tile [S, k], tiles [n_tiles, 4], nt)."""
+    import torch
+    s = blk.shape
+    S, k, E = s.S, s.k, s.E
+    st = moe.read_region(s, blk.ws, moe.MOE_WS_STATUS, torch.int32).numpy()
+    pos = moe.read_region(s, blk.ws, moe.MOE_WS_POS, torch.int32).numpy()
+    n_tiles = int(st[3])
+    tiles = moe.read_region(s, blk.ws, moe.MOE_WS_TILES, torch.int32).numpy().reshape(-1, 4)[:n_tiles]
+    nt = _tile_picks(mi.MoEConfig("x", S=S, d=s.d, E=E, k=k, I=s.I))
+    assert int(st[2]) == S * k
+    cnt = np.bincount(ids.ravel(), minlength=E)
+    seg = np.concatenate([[0], np.cumsum(cnt)])
+    flat_ids = ids.ravel()
+    # positions: a permutation of 0..P-1 with expert e's picks in its segment
+    assert np.array_equal(np.sort(pos), np.arange(S * k))
+    assert np.all(pos >= seg[flat_ids]) and np.all(pos < seg[flat_ids + 1])
+    # tiles: expert e's segment in order, nt picks each but the last
+    want = [(e, seg[e] + i, min(nt, cnt[e] - i)) for e in range(E) for i in range(0, cnt[e], nt)]
+    got = sorted((int(t[0]), int(t[1]), int(t[2])) for t in tiles)
+    assert got == sorted(want)
+    pos2tile = np.empty(S * k, np.int64)
+    for ti, (e, p0, n, _) in enumerate(tiles):
+        pos2tile[p0:p0 + n] = ti
+    tile = pos2tile[pos]
+    slot = pos - tiles[tile, 1]
+    return slot.reshape(S, k), tile.reshape(S, k), tiles, nt
+
+
+def _cover_rows(ids, slot, tile, targets_of, min_rows, seed=0):
+    """Token rows whose picks cover every target (greedy: most new targets
+    first, then fewest experts the oracle has not dequantised yet), topped up
+    to min_rows with rows that add as few experts as possible."""
+    S = ids.shape[0]
+    rng = np.random.default_rng(seed)
+    cov = [set(targets_of(t)) for t in range(S)]
+    need = set().union(*cov)
+    chosen, experts = [], set()
+    while need:
+        best = max(range(S), key=lambda t: (len(cov[t] & need), -len(set(ids[t]) - experts)))
+        assert cov[best] & need
+        chosen.append(best)
+        need -= cov[best]
+        experts |= set(ids[best])
+    rest = [t for t in rng.permutation(S) if t not in chosen]
+    rest.sort(key=lambda t: len(set(ids[t]) - experts))
+    for t in rest:
+        if len(chosen) >= min_rows:
+            break
+        chosen.append(int(t))
+        experts |= set(ids[t])
+    return sorted(chosen)
+
+
+def _full_size_parity(ci, min_rows, hot_targets):
+    cfg = mi.CONFIGS[ci]
     inp = mi.make_inputs(cfg)
-    ids, w, out = gpu_forward(inp)
-    # every token's routing exactly; outputs on a sample of tokens
+    blk = device_block(inp)
+    ids_t, w_t, out_t = blk.forward()
+    moe.check_device_status(blk.ws, "forward")
+    ids, w, out = ids_t.cpu().numpy(), w_t.cpu().numpy(), out_t.cpu().numpy().astype(np.float64)
+    # every token's routing exactly
     L = O.router_logits(inp.x, inp.w_gate, inp.logit_off)
     rids, rw = O.route(L, inp.bias, cfg.k)
     assert np.array_equal(ids, rids)
     assert np.max(np.abs(w - rw) / rw) <= W_TOL
-    _check(inp, ids, w, out, rows=[0, 17, 63, 64, 100, 127])
+    slot, tile, tiles, nt = _sort_state(blk, ids)
+    extra = hot_targets(ids, tiles, nt)
+
+    def targets_of(t):
+        tg = {("slot", int(s)) for s in slot[t]}
+        tg |= {("tile", int(ti)) for ti in tile[t] if ("tile", int(ti)) in extra}
+        tg |= {("chunk", int(ti), int(s) // 16) for ti, s in zip(tile[t], slot[t])
+               if ("chunk", int(ti), int(s) // 16) in extra}
+        return tg
+
+    rows = _cover_rows(ids, slot, tile, targets_of, min_rows)
+    covered = set().union(*(targets_of(t) for t in rows))
+    assert {("slot", s) for s in range(nt)} <= covered and extra <= covered
+    assert len(rows) >= min_rows
+    _check(inp, ids, w, out, rows=rows)
+    return rows, nt
 
 
-def test_config4_sampled():
-    cfg = mi.CONFIGS[4]
-    inp = mi.make_inputs(cfg)
-    ids, w, out = gpu_forward(inp)
-    L = O.router_logits(inp.x, inp.w_gate, inp.logit_off)
-    rids, rw = O.route(L, inp.bias, cfg.k)
-    assert np.array_equal(ids, rids)
-    assert np.max(np.abs(w - rw) / rw) <= W_TOL
-    _check(inp, ids, w, out, rows=[0, 1, 2047, 4095])
+def test_config3_full_size_tiles():
+    """S = 128 (16-pick tiles, per-pick norm): the checked rows cover every
+    tile slot and every tile of each expert that got more than one."""
+    def multi_tile(ids, tiles, nt):
+        per_e = {}
+        for ti, t in enumerate(tiles):
+            per_e.setdefault(int(t[0]), []).append(ti)
+        return {("tile", ti) for tis in per_e.values() if len(tis) > 1 for ti in tis}
+
+    rows, nt = _full_size_parity(3, 32, multi_tile)
+    assert nt == 16
+
+
+def test_config4_full_size_tiles():
+    """S = 4096 (64-pick tiles, Zipf-skewed experts): the checked rows cover
+    every tile slot (so every 16-pick epilogue chunk), the last tile of the
+    hottest expert (partial unless its picks are a multiple of 64) and every
+    chunk of one of its middle tiles."""
+    def hottest(ids, tiles, nt):
+        cnt = np.bincount(ids.ravel())
+        e = int(np.argmax(cnt))
+        tis = sorted((int(t[1]), ti) for ti, t in enumerate(tiles) if int(t[0]) == e)
+        assert len(tis) >= 3, "the hottest expert has a middle tile"
+        mid = tis[len(tis) // 2][1]
+        # and the last tile of every expert that got more than one
+        per_e = {}
+        for ti, t in enumerate(tiles):
+            per_e.setdefault(int(t[0]), []).append((int(t[1]), ti))
+        multi = {("tile", max(v)[1]) for v in per_e.values() if len(v) > 1}
+        return {("tile", tis[-1][1])} | {("chunk", mid, c) for c in range(nt // 16)} | multi
+
+    rows, nt = _full_size_parity(4, 64, hottest)
+    assert nt == 64
 
 
 SMALL = [
