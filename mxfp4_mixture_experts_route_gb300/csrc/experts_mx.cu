@@ -79,6 +79,9 @@ constexpr int A_TX = AROWS * KS / 2;         // packed bytes of a weight tile: t
 #ifndef MOE_MX_WIDE_TOKEN_STAGES
 #define MOE_MX_WIDE_TOKEN_STAGES 3
 #endif
+#ifndef MOE_MX_DOWN_BLOCKS
+#define MOE_MX_DOWN_BLOCKS 2
+#endif
 constexpr int NSB_DEF = MOE_MX_TOKEN_STAGES; // token-tile stages (MOE_MX_WIDE_TOKEN_STAGES for 64-pick tiles)
 constexpr int TMEM_COLS = 512;
 constexpr int NMMA_MAX = 2;                  // MMA-issuing warps (one thread each; one for 64-pick tiles)
@@ -94,6 +97,24 @@ constexpr int NUM_WARPS = 13;
 constexpr int LOOKAHEAD = 2;                 // units the scheduler publishes ahead of the weight producer
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 constexpr int UR = 32;                       // unit ring entries
+// Diagnostics build (-DMOE_TRACE): %globaltimer stamps per CTA, read back
+// with moe_trace_copy: [cta][TR_KINDS][TR_CAP] u64, kinds below (index = the
+// CTA's stage or unit sequence number; slot 0 of TR_MISC = kernel start, 1 =
+// after the wait on the preceding kernel, 2 = end).
+#ifdef MOE_TRACE
+constexpr int TR_CAP = 1024, TR_KINDS = 8, TR_MAX_CTAS = 160;
+enum { TR_UNIT = 0, TR_ISSUE = 1, TR_LANDED = 2, TR_MMA = 3, TR_MISC = 4, TR_UDESC = 5, TR_ACCE = 6, TR_EPI = 7 };
+__device__ uint64_t g_trace[TR_MAX_CTAS][TR_KINDS][TR_CAP];
+#define MOE_TR(kind, idx)                                                                    \
+    do {                                                                                     \
+        if (blockIdx.x < TR_MAX_CTAS && (idx) < TR_CAP) g_trace[blockIdx.x][kind][idx] = ptx::globaltimer(); \
+    } while (0)
+#else
+#define MOE_TR(kind, idx) \
+    do {                  \
+    } while (0)
+#endif
+
 #ifndef MOE_WAIT_TEST
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 #else
@@ -116,13 +137,22 @@ struct Cfg {
     static constexpr int B_SLAB = NB * 128;                    // one 128-K slab of the token tile
     static constexpr int B_SMEM = 2 * B_SLAB;                  // a token stage (4 or 8 KB)
     static constexpr int BS_BYTES = NTT * TOKEN_SCALE_ROW;     // the tile's token scale rows
-    // fp32 accumulators: ACCB buffers (by unit) x NMMA issuers x NB columns; 4
-    // buffers when they fit beside six scale slots, so that short units do not
-    // wait for the epilogue to drain the buffer of two units back
-    static constexpr int ACCB = NTT == 8 ? 4 : 2;
+    // 128-row blocks of w2 in one down unit: a down unit is short (I / 256
+    // stages a block), and every unit costs a claim, a tile-entry read and a
+    // readiness check of its h rows; several blocks of one tile can share
+    // them where the accumulators fit in TMEM beside the scale slots
+    static constexpr int RD = NTT == 8 ? MOE_MX_DOWN_BLOCKS : 1;
+    // fp32 accumulators: ACCB buffers (by unit) of RD x NMMA accumulators of
+    // NB columns: block b of the unit, issuer slot j (the issuers take
+    // alternate stages of a block); 4 buffers when they fit beside six scale
+    // slots, so that short units do not wait for the epilogue to drain the
+    // buffer of two units back
+    static constexpr int ACC_UNIT = RD * NMMA;
+    static constexpr int BW = ACC_UNIT * NB;
+    static constexpr int ACCB = (NTT == 8 && RD == 1) ? 4 : 2;
     static constexpr int BSG = (NB + 31) / 32;                 // TMEM columns of one group of token scales
     static_assert(NTT <= NT_MAX, "token tables are padded by NT_MAX rows");
-    static constexpr int SF_COL0 = ACCB * NMMA * NB;           // TMEM columns of the scale slots
+    static constexpr int SF_COL0 = ACCB * BW;                  // TMEM columns of the scale slots
 
     static constexpr int SC_ROW = STMA ? 16 : 8;               // e8m0 bytes of a row in a stage
     static constexpr int SC_BYTES = AROWS * SC_ROW;
@@ -174,15 +204,16 @@ __device__ __forceinline__ Tile load_tile(const Tile* p) {
 
 struct Unit {
     int down;        // 0: gate_up, 1: down, -1: no more units
-    int tile, mb;    // tile index and row block
+    int tile, mb;    // tile index; row block (gate_up) or group of RD row blocks (down)
     int e, p0, n;
     int stages;      // 256-K stages of the unit
-    int pad;
+    int nblk;        // down: 128-row blocks of the unit (<= RD)
 };
 
-// unit u of the call (u < U1: gate_up units, tile-major; then down units)
-__device__ __forceinline__ void unit_coords(int u, int U1, const Args& a, int& down, int& tile, int& mb) {
-    const int mb1 = a.I / 64, mb2 = a.d / AROWS;
+// unit u of the call (u < U1: gate_up units, tile-major; then down units, g2
+// groups of rd row blocks a tile)
+__device__ __forceinline__ void unit_coords(int u, int U1, int g2, const Args& a, int& down, int& tile, int& mb) {
+    const int mb1 = a.I / 64;
     if (u < U1) {
         down = 0;
         tile = u / mb1;
@@ -190,18 +221,34 @@ __device__ __forceinline__ void unit_coords(int u, int U1, const Args& a, int& d
     } else {
         const int v = u - U1;
         down = 1;
-        tile = v / mb2;
-        mb = v % mb2;
+        tile = v / g2;
+        mb = v % g2;
     }
 }
 
-// global row (in the [E * rows, K/2] view) of weight row r (0..127) of unit U
-__device__ __forceinline__ int weight_row(const Unit& U, int r, const Args& a) {
+// Walks the stages of a unit in order: stage c is 256-K stage kc of the
+// unit's 128-row block blk (down units: kst stages a block; gate_up units:
+// one block, kc = c).  Incremental, so that the per-stage loops of the
+// pipeline's roles carry no division.
+struct StageWalk {
+    int blk = 0, kc = 0, kst;
+    __device__ __forceinline__ explicit StageWalk(const Unit& U, int kst_down) : kst(U.down ? kst_down : 1 << 30) {}
+    __device__ __forceinline__ void next() {
+        if (++kc == kst) {
+            kc = 0;
+            ++blk;
+        }
+    }
+};
+
+// global row (in the [E * rows, K/2] view) of weight row r (0..127) of block
+// blk of unit U (rd row blocks a down unit)
+__device__ __forceinline__ int weight_row(const Unit& U, int blk, int r, int rd, const Args& a) {
     if (!U.down) {
         const int base = U.e * 2 * a.I + U.mb * 64;
         return r < 64 ? base + r : base + a.I + (r - 64);
     }
-    return U.e * a.d + U.mb * AROWS + r;
+    return U.e * a.d + (U.mb * rd + blk) * AROWS + r;
 }
 
 template <bool STMA, int NTT>
@@ -213,6 +260,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     using C = Cfg<STMA, NTT>;
     constexpr int NSA = C::NSA, NB = C::NB, B_SLAB = C::B_SLAB, B_SMEM = C::B_SMEM, BS_BYTES = C::BS_BYTES;
     constexpr int SF_COL0 = C::SF_COL0, ACCB = C::ACCB, NSB = C::NSB, NMMA = C::NMMA, EC = C::EC;
+    constexpr int RD = C::RD, BW = C::BW;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* wst = smem;                                  // weight stages [NSA][A_STAGE]
@@ -225,26 +273,32 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     uint64_t* empty_a = full_a + NSA;       // [NSA] both issuers done with the weight stage
     uint64_t* full_b = empty_a + NSA;       // [NSB] token tile + its scales landed
     uint64_t* empty_b = full_b + NSB;       // [NSB] both issuers done with the token stage
-    uint64_t* sf_full = empty_b + NSB;      // [NSA] the stage's scales are in TMEM
-    uint64_t* acc_full = sf_full + NSA;     // [ACCB]
+    // [NMMA_MAX][NSA] the stage's scales are in TMEM: one barrier per issuer
+    // and slot, arrived on for the stages that issuer owns, so that each issuer
+    // waits on the phases of its own barriers strictly in order (an issuer
+    // skips the other's stages; a shared barrier could be a full phase ahead
+    // of it, which a parity wait cannot tell from the phase it wants)
+    uint64_t* sf_full = empty_b + NSB;
+    uint64_t* acc_full = sf_full + NMMA_MAX * NSA;   // [ACCB]
     uint64_t* acc_empty = acc_full + ACCB;  // [ACCB]
     uint64_t* u_full = acc_empty + ACCB;    // [UR]
     uint64_t* u_empty = u_full + UR;        // [UR]
     uint64_t* fin = u_empty + UR;           // [NMMA_MAX]
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(fin + NMMA_MAX);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(tmem_holder + 1);
-    volatile int* epi_flag = abort_flag + 1;
-    volatile int* taken = abort_flag + 2;   // units the weight producer has taken
+    volatile int* taken = abort_flag + 1;   // units the weight producer has taken
+    volatile int* epi_flag = abort_flag + 2;   // [2] the epilogue's leave decision, by unit parity
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     StatusBlock* sb = a.sb;
+    if (threadIdx.x == 0) MOE_TR(TR_MISC, 0);
     pdl_trigger();
 
     if (threadIdx.x == 0) {
         for (int i = 0; i < NSA; ++i) {
             ptx::mbar_init(&full_a[i], STMA ? 1 : 1 + 32);   // expect_tx (+ 32 cp.async arrivals)
             ptx::mbar_init(&empty_a[i], 1);                 // the stage's issuer
-            ptx::mbar_init(&sf_full[i], 4);                 // the four scale movers
+            for (int m = 0; m < NMMA_MAX; ++m) ptx::mbar_init(&sf_full[m * NSA + i], 4);   // the four scale movers
         }
         for (int i = 0; i < NSB; ++i) {
             ptx::mbar_init(&full_b[i], 1);
@@ -279,6 +333,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // the set-up above needs nothing from the preceding kernels; everything
     // below reads their results
     pdl_wait();
+    if (threadIdx.x == 0) MOE_TR(TR_MISC, 1);
     // CTA b's first unit is unit b; the later ones are claimed from the counter
     // (offset by the grid size).  The tile count, the first unit's tile entry
     // (read as if it were a gate_up unit, the usual case, and read again below
@@ -296,6 +351,9 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const uint32_t tmem = *tmem_holder;
 
     const int mb1 = a.I / 64;
+    const int kst_down = (a.I + KS - 1) / KS;             // 256-K stages of one down row block
+    const int mb2 = a.d / AROWS;                          // 128-row blocks of w2 per expert
+    const int g2 = (mb2 + RD - 1) / RD;                   // down units per tile
 
     auto fail = [&](int site) {
         latch_status(sb, MOE_ERR_TIMEOUT, site);
@@ -322,10 +380,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             if (lane == 0) *taken = i + 1;
+            if (lane == 0) MOE_TR(TR_UNIT, i);
+#ifdef MOE_TRACE
+            if (lane == 0 && blockIdx.x < TR_MAX_CTAS && i < TR_CAP)
+                g_trace[blockIdx.x][TR_UDESC][i] = 1ull << 63 | (uint64_t)(U.down + 1) << 48 |
+                                                   (uint64_t)U.tile << 24 | (uint64_t)U.mb << 8 | (uint64_t)U.stages;
+#endif
             if (U.down < 0) break;
             const int K = U.down ? a.I : a.d;
-            const int r0 = U.down ? U.e * a.d + U.mb * AROWS : U.mb * 64;
-            for (int c = 0; c < U.stages; ++c, ++ts) {
+            StageWalk sa(U, kst_down);
+            for (int c = 0; c < U.stages; ++c, ++ts, sa.next()) {
+                const int r0 = U.down ? U.e * a.d + (U.mb * RD + sa.blk) * AROWS : U.mb * 64;
                 const int s = ts % NSA;
                 if (!ptx::mbar_wait_warp(&empty_a[s], ((ts / NSA) & 1) ^ 1, abort_flag, WAIT_NS)) {
                     if (lane == 0) fail(1);
@@ -334,14 +399,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 uint8_t* st = wst + s * C::A_STAGE;
                 if (lane == 0) {
+                    MOE_TR(TR_ISSUE, ts);
                     ptx::mbar_arrive_expect_tx(&full_a[s], A_TX + (STMA ? C::SC_BYTES : 0));
                     if (!U.down) {
                         // gate rows mb*64.. and up rows I + mb*64.. of expert e, 2 slabs of 128 K
-                        ptx::tma_load_4d(st, &tm_w13, 0, r0, 2 * U.e, 2 * c, &full_a[s], pol_w);
-                        if (STMA) ptx::tma_load_3d(st + C::SC_OFF, &tm_w13s, (c >> 1) * 16, r0, 2 * U.e, &full_a[s], pol_w);
+                        ptx::tma_load_4d(st, &tm_w13, 0, r0, 2 * U.e, 2 * sa.kc, &full_a[s], pol_w);
+                        if (STMA) ptx::tma_load_3d(st + C::SC_OFF, &tm_w13s, (sa.kc >> 1) * 16, r0, 2 * U.e, &full_a[s], pol_w);
                     } else {
-                        ptx::tma_load_3d(st, &tm_w2, 0, r0, 2 * c, &full_a[s], pol_w);
-                        if (STMA) ptx::tma_load_2d(st + C::SC_OFF, &tm_w2s, (c >> 1) * 16, r0, &full_a[s], pol_w);
+                        ptx::tma_load_3d(st, &tm_w2, 0, r0, 2 * sa.kc, &full_a[s], pol_w);
+                        if (STMA) ptx::tma_load_2d(st + C::SC_OFF, &tm_w2s, (sa.kc >> 1) * 16, r0, &full_a[s], pol_w);
                     }
                 }
                 if (!STMA) {
@@ -353,10 +419,10 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 #pragma unroll
                     for (int j = 0; j < 4; ++j) {
                         const int r = lane + 32 * j;
-                        const uint8_t* row = sbase + (size_t)weight_row(U, r, a) * kb;
+                        const uint8_t* row = sbase + (size_t)weight_row(U, sa.blk, r, RD, a) * kb;
 #pragma unroll
                         for (int hh = 0; hh < 2; ++hh) {
-                            const int sub = 2 * c + hh;
+                            const int sub = 2 * sa.kc + hh;
                             ptx::cp_async_4(st + C::SC_OFF + 8 * r + 4 * hh, row + (sub * 4 < kb ? sub * 4 : 0));
                         }
                     }
@@ -369,31 +435,37 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     } else if (warp == SCHED_WARP) {
         // ------------------------------------------------------------ unit scheduler
         const int U1 = n_tiles * mb1;
-        const int total = U1 + n_tiles * (a.d / AROWS);
-        auto tile_of = [&](int u) { return u < U1 ? u / mb1 : (u - U1) / (a.d / AROWS); };
-        // unit u and its tile entry; the claim of the next unit is in flight
-        // while this one waits for its turn.  A claim is kept as the raw counter
-        // value until it is used: arithmetic on it would wait for the atomic.
+        const int total = U1 + n_tiles * g2;
+        auto tile_of = [&](int u) { return u < U1 ? u / mb1 : (u - U1) / g2; };
+        // Unit u and its tile entry; the claim of the next unit and its tile
+        // entry are in flight while this one waits for its turn (a claim is
+        // kept as the raw counter value until it is used: arithmetic on it
+        // would wait for the atomic).  The CTA's first unit is published
+        // before that, so that its weights stream without waiting for a claim.
         int u = (int)blockIdx.x;
         int next_claim = claim1;   // lane 0
         Tile tl = tile0, tl_next = {0, 0, 0, 0};
+        int u_next = total;
         if (u >= U1 && u < total) tl = load_tile(a.tiles + tile_of(u));
+        auto claim_next = [&]() {
+            u_next = u < total ? (int)gridDim.x + __shfl_sync(0xffffffffu, next_claim, 0) : total;
+            if (u_next < total) tl_next = load_tile(a.tiles + tile_of(u_next));
+            if (lane == 0) next_claim = u_next < total ? atomicAdd(&sb->work_next, 1) : total;
+        };
         for (int i = 0;; ++i) {
             Unit U;
             if (u < total) {
-                unit_coords(u, U1, a, U.down, U.tile, U.mb);
+                unit_coords(u, U1, g2, a, U.down, U.tile, U.mb);
                 U.e = tl.e;
                 U.p0 = tl.p0;
                 U.n = tl.n;
-                U.stages = ((U.down ? a.I : a.d) + KS - 1) / KS;
+                U.nblk = U.down ? min(RD, mb2 - U.mb * RD) : 0;
+                U.stages = U.down ? U.nblk * kst_down : (a.d + KS - 1) / KS;
             } else {
                 U.down = -1;
-                U.tile = U.mb = U.e = U.p0 = U.n = U.stages = 0;
+                U.tile = U.mb = U.e = U.p0 = U.n = U.stages = U.nblk = 0;
             }
-            U.pad = 0;
-            const int u_next = u < total ? (int)gridDim.x + __shfl_sync(0xffffffffu, next_claim, 0) : total;
-            if (u_next < total) tl_next = load_tile(a.tiles + tile_of(u_next));
-            if (lane == 0) next_claim = u_next < total ? atomicAdd(&sb->work_next, 1) : total;
+            if (i > 0) claim_next();
             // publish unit i once the weight producer has taken unit i - LOOKAHEAD
             // (bounded): claimed units wait in this CTA for a short while only
             bool go = true;
@@ -419,6 +491,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::mbar_arrive(&u_full[i % UR]);
             }
             if (U.down < 0) break;
+            if (i == 0) claim_next();
             u = u_next;
             tl = tl_next;
         }
@@ -461,7 +534,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
                 if (!__shfl_sync(0xffffffffu, ready, 0)) break;
             }
-            for (int c = 0; c < U.stages; ++c, ++ts) {
+            StageWalk sw(U, kst_down);
+            for (int c = 0; c < U.stages; ++c, ++ts, sw.next()) {
                 const int s = ts % NSB;
                 if (!ptx::mbar_wait_warp(&empty_b[s], ((ts / NSB) & 1) ^ 1, abort_flag, WAIT_NS)) {
                     if (lane == 0) fail(13);
@@ -469,10 +543,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     break;
                 }
                 if (lane == 0) {
+                    // a down unit's blocks read the same h rows: stage kc of h
+                    const int kc = sw.kc;
                     uint8_t* st = tst + s * C::B_STAGE;
                     ptx::mbar_arrive_expect_tx(&full_b[s], B_SMEM + BS_BYTES);
-                    ptx::tma_load_3d(st, tmB, 0, 2 * U.p0, 2 * c, &full_b[s], pol_x);
-                    ptx::bulk_load(tsc + s * BS_BYTES, tab + ((size_t)c * tab_rows + U.p0) * TOKEN_SCALE_ROW,
+                    ptx::tma_load_3d(st, tmB, 0, 2 * U.p0, 2 * kc, &full_b[s], pol_x);
+                    ptx::bulk_load(tsc + s * BS_BYTES, tab + ((size_t)kc * tab_rows + U.p0) * TOKEN_SCALE_ROW,
                                    BS_BYTES, &full_b[s], pol_x);
                 }
                 __syncwarp();
@@ -492,7 +568,8 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             if (U.down < 0) break;
-            for (int c = 0; c < U.stages; ++c, ++ts) {
+            StageWalk sa(U, kst_down);
+            for (int c = 0; c < U.stages; ++c, ++ts, sa.next()) {
                 const int s = ts % NSA, sbi = ts % NSB;
                 if (!ptx::mbar_wait_warp(&full_a[s], (ts / NSA) & 1, abort_flag, WAIT_NS) ||
                     !ptx::mbar_wait_warp(&full_b[sbi], (ts / NSB) & 1, abort_flag, WAIT_NS)) {
@@ -500,8 +577,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     ok = false;
                     break;
                 }
+                if (q == 0 && lane == 0) MOE_TR(TR_LANDED, ts);
                 const uint8_t* st = wst + s * C::A_STAGE;
-                const uint2 wa = *reinterpret_cast<const uint2*>(st + C::SC_OFF + C::SC_ROW * r + (STMA ? 8 * (c & 1) : 0));
+                const int kc = sa.kc;
+                const int owner = c % NMMA;   // the stage's MMA issuer
+                const uint2 wa = *reinterpret_cast<const uint2*>(st + C::SC_OFF + C::SC_ROW * r + (STMA ? 8 * (kc & 1) : 0));
                 // token column n = 32 g + lane (g < BSG): pick n / 2 (its hi and lo
                 // row); columns past the tile's 2 NTT are never read
                 uint32_t bx[C::BSG], by[C::BSG];
@@ -537,7 +617,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 ptx::tmem_st_wait();
                 ptx::tc_fence_before();
                 __syncwarp();
-                if (lane == 0) ptx::mbar_arrive(&sf_full[s]);
+                if (lane == 0) ptx::mbar_arrive(&sf_full[owner * NSA + s]);
             }
         }
     } else if (warp >= MMA_WARP0 && warp < MMA_WARP0 + NMMA) {
@@ -549,6 +629,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         // both TMA copies are complete and visible once sf_full completes.
         const int m = warp - MMA_WARP0;
         int ts = 0;
+        uint32_t sf_par = 0;   // bit s: parity of the next phase of this issuer's sf_full[s]
         for (int i = 0;; ++i) {
             Unit U;
             if (!take_unit(i, U)) {
@@ -559,20 +640,30 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             bool ok = true;
             if (lane == 0) {
                 const int ab = i % ACCB;
-                const uint32_t d_tmem = tmem + (ab * NMMA + m) * NB;
-                for (int c = 0; c < U.stages; ++c, ++ts) {
+                // every issuer waits for the accumulator buffer of every unit
+                // (drained by the epilogue ACCB units back), also when it has no
+                // stage in it, so that it never waits two phases ahead
+                if (!ptx::mbar_wait(&acc_empty[ab], ((i / ACCB) & 1) ^ 1, abort_flag, WAIT_NS)) {
+                    fail(3);
+                    ok = false;
+                }
+                if (m == 0) MOE_TR(TR_ACCE, i);
+                StageWalk sa(U, kst_down);
+                for (int c = 0; ok && c < U.stages; ++c, ++ts, sa.next()) {
+                    // issuer m takes the stages c = m (mod NMMA) of the unit; stage
+                    // kc of row block b goes to accumulator slot kc mod NMMA of the
+                    // block (every stage of a slot has the same issuer)
                     if (c % NMMA != m) continue;
+                    const uint32_t d_tmem = tmem + ab * BW + (sa.blk * NMMA + sa.kc % NMMA) * NB;
+                    const bool acc = sa.kc >= NMMA;
                     const int s = ts % NSA, sbi = ts % NSB;
-                    if (c == m && !ptx::mbar_wait(&acc_empty[ab], ((i / ACCB) & 1) ^ 1, abort_flag, WAIT_NS)) {
-                        fail(3);
-                        ok = false;
-                        break;
-                    }
-                    if (!ptx::mbar_wait(&sf_full[s], (ts / NSA) & 1, abort_flag, WAIT_NS)) {
+                    if (!ptx::mbar_wait(&sf_full[m * NSA + s], (sf_par >> s) & 1u, abort_flag, WAIT_NS)) {
                         fail(4);
                         ok = false;
                         break;
                     }
+                    sf_par ^= 1u << s;
+                    MOE_TR(TR_MMA, ts);
                     ptx::tc_fence_after();
                     const uint32_t a0 = ptx::smem_u32(wst + s * C::A_STAGE);
                     const uint32_t b0 = ptx::smem_u32(tst + sbi * C::B_STAGE);
@@ -582,7 +673,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         const int h = kk >> 2, j = kk & 3;   // 128-K slab, K step within it
                         ptx::mma_mx_ss(d_tmem, ptx::smem_desc_sw128(a0 + h * A_SLAB + 32 * j),
                                        ptx::smem_desc_sw128(b0 + h * B_SLAB + 32 * j),
-                                       ptx::idesc_mx_e2m1_e4m3(AROWS, NB, j, j), (c > m || kk > 0) ? 1u : 0u,
+                                       ptx::idesc_mx_e2m1_e4m3(AROWS, NB, j, j), (acc || kk > 0) ? 1u : 0u,
                                        tmem + col + SF_A1 * h, tmem + col + SF_B0 + (SF_B1 - SF_B0) * h);
                     }
                     ptx::mma_commit(&empty_a[s]);
@@ -621,38 +712,62 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (!end && !*abort_flag && !ptx::mbar_wait_warp(&acc_full[ab], (i / ACCB) & 1, abort_flag, WAIT_NS) &&
                 lane == 0)
                 fail(7);
+            // one barrier a unit: the decision flags alternate, so that a flag
+            // is written again only after every warp has passed the next barrier
+            if (threadIdx.x == EPI_WARP0 * 32) epi_flag[i & 1] = *abort_flag;
             ptx::named_bar_sync(1, 128);
-            if (threadIdx.x == EPI_WARP0 * 32) *epi_flag = *abort_flag;
-            ptx::named_bar_sync(1, 128);
-            if (*epi_flag || end) break;
+            if (epi_flag[i & 1] || end) break;
+            if (threadIdx.x == EPI_WARP0 * 32) MOE_TR(TR_EPI, i);
             ptx::tc_fence_after();
-            const int n_iss = U.stages < NMMA ? U.stages : NMMA;   // issuers that had a stage
-            const int ii = U.mb * 64 + r;        // gate_up: h row of lanes 0..63
-            const int blk = ii / 32;             // its 32-row block of h
-            // the tile's picks in chunks of EC: v[n] = the issuers' stages, hi + lo
-            // column of pick ch + n
-#pragma unroll 1
-            for (int ch = 0; ch < NTT; ch += EC) {
-                float v[EC];
+            // accumulators of a row block: one per issuer slot that had a stage
+            // in the block, added
+            const int kst_blk = U.down ? kst_down : U.stages;
+            const int nacc = kst_blk < NMMA ? kst_blk : NMMA;
+            // the tile's picks in chunks of EC: v[n] = the block's accumulators,
+            // hi + lo column of pick ch + n (8-pick chunks: every TMEM load in
+            // flight before one wait; wider chunks one accumulator at a time,
+            // within the registers a thread has)
+            auto read_chunk = [&](uint32_t acc_col, int ch, float (&v)[EC]) {
+                constexpr int NL = EC <= 8 ? NMMA : 1;   // accumulators loaded before a wait
 #pragma unroll
                 for (int n = 0; n < EC; ++n) v[n] = 0.f;
 #pragma unroll
-                for (int mm = 0; mm < NMMA; ++mm) {
-                    if (mm >= n_iss) break;
-                    uint32_t t[2 * EC];
+                for (int m0 = 0; m0 < NMMA; m0 += NL) {
+                    if (m0 >= nacc) break;
+                    uint32_t t[NL][2 * EC];
 #pragma unroll
-                    for (int j = 0; j < 2 * EC / 16; ++j)
-                        ptx::tmem_ld16(tmem + lane_base + (ab * NMMA + mm) * NB + 2 * ch + 16 * j, t + 16 * j);
+                    for (int mm = 0; mm < NL; ++mm) {
+                        if (m0 + mm < nacc) {
+#pragma unroll
+                            for (int j = 0; j < 2 * EC / 16; ++j)
+                                ptx::tmem_ld16(tmem + lane_base + acc_col + (m0 + mm) * NB + 2 * ch + 16 * j,
+                                               t[mm] + 16 * j);
+                        }
+                    }
                     ptx::tmem_ld_wait();
 #pragma unroll
-                    for (int n = 0; n < EC; ++n) v[n] += __uint_as_float(t[2 * n]) + __uint_as_float(t[2 * n + 1]);
+                    for (int mm = 0; mm < NL; ++mm) {
+                        if (m0 + mm < nacc) {
+#pragma unroll
+                            for (int n = 0; n < EC; ++n)
+                                v[n] += __uint_as_float(t[mm][2 * n]) + __uint_as_float(t[mm][2 * n + 1]);
+                        }
+                    }
                 }
-                if (ch + EC >= NTT) {   // the accumulator is read out
-                    ptx::tc_fence_before();
-                    __syncwarp();
-                    if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);
-                }
-                if (!U.down) {
+            };
+            auto release_acc = [&]() {   // the unit's accumulators are read out
+                ptx::tc_fence_before();
+                __syncwarp();
+                if (lane == 0) ptx::mbar_arrive(&acc_empty[ab]);
+            };
+            if (!U.down) {
+                const int ii = U.mb * 64 + r;        // h row of lanes 0..63
+                const int blk = ii / 32;             // its 32-row block of h
+#pragma unroll 1
+                for (int ch = 0; ch < NTT; ch += EC) {
+                    float v[EC];
+                    read_chunk(ab * BW, ch, v);
+                    if (ch + EC >= NTT) release_acc();
                     // lanes 0..63: gate of rows mb*64 + r; lanes 64..127: up of the same rows
                     if (r >= 64) {
 #pragma unroll
@@ -698,39 +813,56 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                         }
                     }
                     ptx::named_bar_sync(1, 128);   // xch is written again by the next chunk
-                } else {
-                    const int m = U.mb * AROWS + r;
+                }
+            } else {
+#pragma unroll 1
+                for (int b = 0; b < U.nblk; ++b) {
+                    const int yrow = (U.mb * RD + b) * AROWS + r;   // row of y
+#pragma unroll 1
+                    for (int ch = 0; ch < NTT; ch += EC) {
+                        float v[EC];
+                        read_chunk(ab * BW + b * NMMA * NB, ch, v);
+                        if (b + 1 == U.nblk && ch + EC >= NTT) release_acc();
 #pragma unroll
-                    for (int n = 0; n < EC; ++n)
-                        if (ch + n < U.n) a.y[(size_t)(U.p0 + ch + n) * a.d + m] = v[n];
-                    if (a.ssq != nullptr) {
-                        // sum of y^2 over the unit's 128 rows for every pick of the
-                        // chunk: a reduce-scatter across the warp (lane l ends with
-                        // pick idx), then (below) the four warps' sums in warp order
-                        float q[EC];
+                        for (int n = 0; n < EC; ++n)
+                            if (ch + n < U.n) a.y[(size_t)(U.p0 + ch + n) * a.d + yrow] = v[n];
+                        if (a.ssq != nullptr) {
+                            // sum of y^2 over the block's 128 rows for every pick of the
+                            // chunk: a reduce-scatter across the warp (lane l ends with
+                            // pick idx), then (below) the four warps' sums in warp order
+                            float q[EC];
 #pragma unroll
-                        for (int n = 0; n < EC; ++n) q[n] = v[n] * v[n];
-                        int idx = 0;
+                            for (int n = 0; n < EC; ++n) q[n] = v[n] * v[n];
+                            int idx = 0;
 #pragma unroll
-                        for (int step = 0; step < 5; ++step) {
-                            const int o = 16 >> step;
-                            const int c = EC >> step;       // values a lane holds before this step
-                            const bool hi = (lane & o) != 0;
-                            if (c > 1) {
+                            for (int step = 0; step < 5; ++step) {
+                                const int o = 16 >> step;
+                                const int c = EC >> step;       // values a lane holds before this step
+                                const bool hi = (lane & o) != 0;
+                                if (c > 1) {
 #pragma unroll
-                                for (int j = 0; j < c / 2; ++j) {
-                                    const float send = hi ? q[j] : q[j + c / 2];
-                                    const float keep = hi ? q[j + c / 2] : q[j];
-                                    q[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                                    for (int j = 0; j < c / 2; ++j) {
+                                        const float send = hi ? q[j] : q[j + c / 2];
+                                        const float keep = hi ? q[j + c / 2] : q[j];
+                                        q[j] = keep + __shfl_xor_sync(0xffffffffu, send, o);
+                                    }
+                                    idx += hi ? c / 2 : 0;
+                                } else {
+                                    q[0] += __shfl_xor_sync(0xffffffffu, q[0], o);
                                 }
-                                idx += hi ? c / 2 : 0;
-                            } else {
-                                q[0] += __shfl_xor_sync(0xffffffffu, q[0], o);
                             }
+                            // every pick's sum now sits on 32 / EC lanes
+                            float* part = xch;                             // [4][NTT]
+                            if ((lane & (32 / EC - 1)) == 0) part[qd * NTT + ch + idx] = q[0];
                         }
-                        // every pick's sum now sits on 32 / EC lanes
-                        float* part = xch;                             // [4][NTT]
-                        if ((lane & (32 / EC - 1)) == 0) part[qd * NTT + ch + idx] = q[0];
+                    }
+                    if (a.ssq != nullptr) {
+                        const float* part = xch;
+                        ptx::named_bar_sync(1, 128);
+                        for (int pr = r; pr < U.n; pr += 128)
+                            a.ssq[(size_t)(U.p0 + pr) * mb2 + (U.mb * RD + b)] =
+                                ((part[pr] + part[NTT + pr]) + part[2 * NTT + pr]) + part[3 * NTT + pr];
+                        ptx::named_bar_sync(1, 128);   // part is written again by the next block or unit
                     }
                 }
             }
@@ -741,17 +873,12 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     __threadfence();
                     ptx::red_release_gpu_add(&a.tile_ready[U.tile], 1u);
                 }
-            } else if (a.ssq != nullptr) {
-                const float* part = xch;
-                ptx::named_bar_sync(1, 128);
-                for (int pr = r; pr < U.n; pr += 128)
-                    a.ssq[(size_t)(U.p0 + pr) * (a.d / AROWS) + U.mb] =
-                        ((part[pr] + part[NTT + pr]) + part[2 * NTT + pr]) + part[3 * NTT + pr];
             }
         }
     }
 
     __syncthreads();
+    if (threadIdx.x == 0) MOE_TR(TR_MISC, 2);
     if (*abort_flag) {
         // let copies still in flight into this CTA's shared memory land
         const uint64_t t0 = ptx::globaltimer();
@@ -882,6 +1009,22 @@ cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p,
 }
 
 }  // namespace moe
+
+#ifdef MOE_TRACE
+// Diagnostics export of the trace build: copies the stamp table to `dst`
+// (host memory, `bytes` <= its size), after synchronising the device.
+// dst == NULL clears the table instead.
+extern "C" int moe_trace_copy(void* dst, size_t bytes) {
+    if (bytes > sizeof(moe::g_trace)) bytes = sizeof(moe::g_trace);
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    if (dst == nullptr) {
+        void* p = nullptr;
+        if (cudaGetSymbolAddress(&p, moe::g_trace) != cudaSuccess) return MOE_ERR_CUDA;
+        return cudaMemset(p, 0, sizeof(moe::g_trace)) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    return cudaMemcpyFromSymbol(dst, moe::g_trace, bytes) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+#endif
 
 #ifdef MOE_WAIT_TEST
 // Test-only export of the wait-test build: on != 0 makes the next launches'
