@@ -93,20 +93,44 @@ def _edge_rows(S, d, rng):
     return bits
 
 
+def _check_rows(xrow, hi, lo, scale_of_block):
+    """One token row x (fp64) against its e4m3 hi / lo rows and block scales."""
+    n_exact = n_below = 0
+    for b in range(len(xrow) // 32):
+        xb = xrow[32 * b:32 * b + 32]
+        M = np.max(np.abs(xb))
+        byte = int(scale_of_block(b))
+        want = 1 if M == 0 else int(np.clip(np.frexp(M)[1] - 1 + 127 - 7, 1, 247))
+        assert byte == want, (b, byte, want)
+        v = (hi[32 * b:32 * b + 32] + lo[32 * b:32 * b + 32]) * 2.0 ** (byte - 127)
+        assert np.all(np.isfinite(v))
+        exact = np.abs(xb) >= M * 2.0 ** -9
+        assert np.array_equal(v[exact], xb[exact]), b
+        assert np.all(np.abs(v[~exact] - xb[~exact]) <= M * 2.0 ** -17), b
+        n_exact += int(exact.sum())
+        n_below += int((~exact).sum())
+    return n_exact, n_below
+
+
+def _edge_block(cfg, seed):
+    inp = mi.make_inputs(cfg)
+    inp.x = _edge_rows(cfg.S, cfg.d, np.random.default_rng(seed))
+    return inp, device_block(inp)
+
+
 @pytest.mark.gpu
 def test_gathered_token_rows_meet_the_precision_claim():
+    """The gather kernel's rows (moe_experts: the picks' rows in sorted order)."""
     import torch
     if not torch.cuda.is_available():
         pytest.skip("no CUDA device")
     ensure_built()
     cfg = mi.CONFIGS[0]           # S = 8, d = 256, E = 8, k = 2
-    inp = mi.make_inputs(cfg)
-    rng = np.random.default_rng(7)
-    inp.x = _edge_rows(cfg.S, cfg.d, rng)
-    blk = device_block(inp)
-    blk.forward()
-    moe.check_device_status(blk.ws, "forward")
+    inp, blk = _edge_block(cfg, 7)
     s = blk.shape
+    moe.route(s, blk.x, blk.w_gate, blk.bias, blk.logit_off, blk.ids, blk.weights, blk.ws)
+    moe.experts(s, blk.x, blk.ids, blk.weights, blk.w13, blk.w13s, blk.w2, blk.w2s, blk.norm_w, blk.out, blk.ws)
+    moe.check_device_status(blk.ws, "route + experts")
     P, d = cfg.S * cfg.k, cfg.d
     pos = moe.read_region(s, blk.ws, moe.MOE_WS_POS, torch.int32).numpy()
     xq = moe.read_region(s, blk.ws, moe.MOE_WS_XQ).numpy().reshape(2 * P, d)
@@ -115,18 +139,8 @@ def test_gathered_token_rows_meet_the_precision_claim():
     n_exact = n_below = 0
     for p in range(P):
         t, r = p // cfg.k, int(pos[p])
-        hi, lo = e4m3_value(xq[2 * r]), e4m3_value(xq[2 * r + 1])
-        for b in range(d // 32):
-            xb = x[t, 32 * b:32 * b + 32]
-            M = np.max(np.abs(xb))
-            byte = int(xs[b // 8, r, b % 8])
-            want = 1 if M == 0 else int(np.clip(np.frexp(M)[1] - 1 + 127 - 7, 1, 247))
-            assert byte == want, (p, b, byte, want)
-            v = (hi[32 * b:32 * b + 32] + lo[32 * b:32 * b + 32]) * 2.0 ** (byte - 127)
-            assert np.all(np.isfinite(v))
-            exact = np.abs(xb) >= M * 2.0 ** -9
-            assert np.array_equal(v[exact], xb[exact]), (p, b)
-            assert np.all(np.abs(v[~exact] - xb[~exact]) <= M * 2.0 ** -17), (p, b)
-            n_exact += int(exact.sum())
-            n_below += int((~exact).sum())
+        e, b = _check_rows(x[t], e4m3_value(xq[2 * r]), e4m3_value(xq[2 * r + 1]),
+                           lambda blk_i: xs[blk_i // 8, r, blk_i % 8])
+        n_exact += e
+        n_below += b
     assert n_exact > 1000 and n_below > 100
