@@ -408,6 +408,34 @@ def per_config_entry(moe, blk, cfg, flush, stream, steps):
     return e
 
 
+def latent_entry(moe, dev, flush, stream, steps: int = 200):
+    """The latent-MoE layer with its shared expert (the K2b layer around the
+    block): route over H, latent down, the routed block at d = LAT, latent norm,
+    up, shared gate/up / activation / down.  Step bytes: the touched experts'
+    MXFP4 weights and scales plus every dense bf16 weight of the layer."""
+    lc = mi.LATENT_CONFIGS[1]
+    inp = mi.make_latent_inputs(lc)
+    shape = moe.LatentShape.of(lc.S, lc.H, lc.LAT, lc.E, lc.k, lc.I, lc.SI, logit_offset=bool(lc.zipf),
+                               norm_eps=lc.norm_eps)
+    blk = moe.DeviceLatentWeights(shape, inp.x, inp.w_gate, inp.bias, inp.logit_off, inp.w_ld, inp.w13,
+                                  inp.w13s, inp.w2, inp.w2s, inp.ln_w, inp.w_up, inp.w_sgu, inp.w_sd, device=dev)
+    ms = timed_steps(blk.forward, steps, flush, stream, warmup=5)
+    moe.check_device_status(blk.ws, "latent steps")
+    n_touched = int(len(np.unique(blk.ids.cpu().numpy())))
+    kmean, ktot, lps = kernel_times(moe, blk.forward, 40, flush)
+    step = statistics.fmean(ms)
+    nbytes = n_touched * mi.expert_weight_bytes(lc.block()) + mi.latent_dense_bytes(lc)
+    hbm, src = measured_peaks()
+    gbs = nbytes / (step * 1e-3) / 1e9
+    return {"workload": lc.name, "S": lc.S, "H": lc.H, "LAT": lc.LAT, "E": lc.E, "k": lc.k, "I": lc.I,
+            "SI": lc.SI, "n_touched": n_touched, "steps": steps, "ms_per_step": step,
+            "ms_per_step_median": statistics.median(ms), "tokens_per_s": lc.S / (step * 1e-3),
+            "step_bytes": nbytes, "step_gbs": gbs, "step_frac_of_hbm": gbs / hbm, "launches_per_step": lps,
+            "kernels_ms": kmean,
+            "what": "latent-MoE layer: route(x) + latent down + routed block at d=LAT + latent RMSNorm + up "
+                    "+ shared expert (bf16 dense products on the tensor cores)"}
+
+
 def run_ours(args, cfg: mi.MoEConfig):
     import torch
     import mxfp4_mixture_experts_route_gb300 as moe
@@ -517,6 +545,8 @@ def run_ours(args, cfg: mi.MoEConfig):
             per_config[c.name] = per_config_entry(moe, ci_blk, c, flush, stream, PER_CONFIG_STEPS[ci])
             prev_inp, prev_blk = ci_inp, ci_blk
         del prev_blk
+        torch.cuda.empty_cache()
+        per_config[mi.LATENT_CONFIGS[1].name] = latent_entry(moe, dev, flush, stream)
 
     cpu = None
     if rank == 0 and not args.no_cpu_baseline:

@@ -238,6 +238,72 @@ int moe_forward_noalloc(const moe_shape* shape, const void* x, const void* w_gat
                         int32_t* status, void* stream);
 
 /*
+ * The latent-MoE layer around the routed block, with a shared expert
+ * (vllm.models.kimi_k3.amd.specialized_decode.mono.layer: K2b's stage list --
+ * router parts and latent parts, route, the shared gate/up and its
+ * activation, ug and down of the routed experts, the shared down, lnorm, up --
+ * and k2_launch's arguments w_gate, bias, w_ld, w_sgu, w_sd, w13, w13s, w2,
+ * w2s, ln_w, w_up, out [S, 7168]).  For token t:
+ *   picks, w_j = the sigmoid top-k of x[t] (as moe_route, over H)
+ *   xl        = x[t] . w_ld^T                   latent input, [LAT] (bf16)
+ *   yl        = sum_j w_j * expert_j(xl)        the routed block at d = LAT
+ *   zl        = yl * rsqrt(mean(yl^2) + norm_eps) * ln_w             (bf16)
+ *   out[t]    = zl . w_up^T  +  (silu(g) * u) . w_sd^T,
+ *               g, u = x[t] . w_sgu[0:SI]^T, x[t] . w_sgu[SI:2SI]^T  (fp32)
+ * The pages give the stages and the argument names, not the formulas or the
+ * formats: the dense weights carry no scale tensors and are bf16 here; the
+ * latent norm is an RMSNorm with weight ln_w; the shared expert is a SwiGLU
+ * expert on the layer input, its output added to the up projection's.  The
+ * intermediate activations xl, zl and silu(g) * u are rounded to bf16, the
+ * operand type of the dense products (bf16 x bf16 on the tensor cores, fp32
+ * accumulation); every sum is fp32.
+ *
+ * Shape: H and LAT multiples of 128 (LAT <= 16384, H <= 16384), SI a
+ * multiple of 128 or 0 (no shared expert), E, k, I as in moe_shape, S * k
+ * <= 1<<20; flags may hold MOE_LOGIT_OFFSET only.
+ */
+typedef struct moe_latent_shape {
+    int32_t S;        /* token rows */
+    int32_t H;        /* hidden size of the layer input and output */
+    int32_t LAT;      /* latent width: the routed experts' d */
+    int32_t E;        /* routed experts */
+    int32_t k;        /* picks per token */
+    int32_t I;        /* routed expert intermediate size */
+    int32_t SI;       /* shared expert intermediate size (0: none) */
+    uint32_t flags;   /* MOE_LOGIT_OFFSET */
+    float norm_eps;   /* latent RMSNorm epsilon */
+} moe_latent_shape;
+
+/* Workspace size of moe_latent_forward in *bytes (pure host function). */
+int moe_latent_workspace_bytes(const moe_latent_shape* shape, size_t* bytes);
+
+/*
+ * The latent-MoE layer, all device pointers (16-byte aligned; w13, w2:
+ * 32-byte aligned), enqueued on `stream`:
+ *   x      [S, H] bf16           w_gate [E, H] bf16     bias [E] fp32
+ *   logit_off [E] fp32 (MOE_LOGIT_OFFSET) or NULL
+ *   w_ld   [LAT, H] bf16         latent down projection
+ *   w13 [E, 2I, LAT/2], w13s [E, 2I, LAT/32], w2 [E, LAT, I/2], w2s
+ *   [E, LAT, I/32]               the routed experts (MXFP4, as moe_experts)
+ *   ln_w   [LAT] fp32            latent norm weight
+ *   w_up   [H, LAT] bf16         up projection
+ *   w_sgu  [2 SI, H] bf16        shared gate (rows 0..SI-1) and up rows
+ *   w_sd   [H, SI] bf16          shared down (both NULL when SI == 0)
+ *   ids, weights [S, k] out      the routing, as moe_route
+ *   out    [S, H] fp32 out       overwritten
+ * ws: at least moe_latent_workspace_bytes(), 256-byte aligned, prepared with
+ * moe_workspace_init.  Errors as for moe_forward.
+ */
+int moe_latent_forward(const moe_latent_shape* shape, const void* x, const void* w_gate,
+                       const float* bias, const float* logit_off, const void* w_ld,
+                       const uint8_t* w13, const uint8_t* w13s,
+                       const uint8_t* w2, const uint8_t* w2s,
+                       const float* ln_w, const void* w_up,
+                       const void* w_sgu, const void* w_sd,
+                       int32_t* ids, float* weights, float* out,
+                       void* ws, size_t ws_bytes, void* stream);
+
+/*
  * Synchronises `stream`, returns the status latched in the workspace by the
  * device since the last call (MOE_OK, MOE_ERR_BAD_IDS, MOE_ERR_BAD_SCALE or
  * MOE_ERR_TIMEOUT; MOE_ERR_CUDA if the synchronisation itself failed) and

@@ -51,6 +51,8 @@ MASK64 = (1 << 64) - 1
 
 # tensor ids of the per-tensor streams
 T_X, T_W_GATE, T_BIAS, T_W13, T_W13S, T_W2, T_W2S, T_NORM_W, T_ZIPF = range(1, 10)
+# the latent-MoE layer's dense weights
+T_W_LD, T_W_UP, T_LN_W, T_W_SGU, T_W_SD = range(10, 15)
 
 # e8m0 bytes 127 + U{-6..-2}
 SCALE_LO, SCALE_N = 121, 5
@@ -302,3 +304,99 @@ def make_inputs(cfg: MoEConfig, seed: int = 0, attempts: np.ndarray | None = Non
 def expert_weight_bytes(cfg: MoEConfig) -> int:
     """Bytes of one expert's w13 + w2 with their e8m0 scales (3 I d 17/32)."""
     return 3 * cfg.I * cfg.d * 17 // 32
+
+
+# ----------------------------------------------------------------------------
+# the latent-MoE layer around the block (k2 page, K2b)
+# ----------------------------------------------------------------------------
+@dataclass(frozen=True)
+class LatentConfig:
+    """One latent-MoE layer workload: S tokens of hidden size H, routed on x;
+    the routed experts work at the latent width LAT (their d); a shared expert
+    of intermediate size SI (0: none)."""
+    name: str
+    S: int
+    H: int
+    LAT: int
+    E: int
+    k: int
+    I: int
+    SI: int
+    zipf: float = 0.0
+    norm_eps: float = 1e-6
+    gap: float = 1e-3
+
+    def router(self) -> MoEConfig:
+        """The routing workload: x [S, H], w_gate [E, H], bias (and the gap)."""
+        return MoEConfig(self.name, S=self.S, d=self.H, E=self.E, k=self.k, I=self.I, zipf=self.zipf,
+                         norm_eps=self.norm_eps, gap=self.gap)
+
+    def block(self) -> MoEConfig:
+        """The routed experts at d = LAT (their w13 / w2 and scales)."""
+        return MoEConfig(self.name + "/experts", S=self.S, d=self.LAT, E=self.E, k=self.k, I=self.I,
+                         norm_eps=self.norm_eps, gap=self.gap)
+
+
+LATENT_CONFIGS = [
+    LatentConfig("latent_tiny", S=8, H=512, LAT=256, E=8, k=2, I=128, SI=128),
+    # the verify-step latent MoE (d = LAT = 4096, I = 512) inside a Kimi-sized
+    # layer (H = 7168) with a shared expert of 2 SI = 1536 gate/up rows
+    LatentConfig("latent_s8_shared", S=8, H=7168, LAT=4096, E=256, k=8, I=512, SI=768),
+]
+
+
+def _normal_bf16(key: int, n: int, std: float) -> np.ndarray:
+    return f32_to_bf16_bits((normal(key, 0, n) * std).astype(np.float32))
+
+
+@dataclass
+class LatentInputs:
+    cfg: LatentConfig
+    seed: int
+    x: np.ndarray                 # [S, H] bf16 bits
+    w_gate: np.ndarray            # [E, H] bf16 bits
+    bias: np.ndarray              # [E] fp32
+    logit_off: np.ndarray | None  # [E] fp32
+    w_ld: np.ndarray              # [LAT, H] bf16 bits
+    w13: np.ndarray               # [E, 2I, LAT/2] uint8
+    w13s: np.ndarray              # [E, 2I, LAT/32] uint8
+    w2: np.ndarray                # [E, LAT, I/2] uint8
+    w2s: np.ndarray               # [E, LAT, I/32] uint8
+    ln_w: np.ndarray              # [LAT] fp32
+    w_up: np.ndarray              # [H, LAT] bf16 bits
+    w_sgu: np.ndarray | None      # [2 SI, H] bf16 bits (gate rows, then up rows)
+    w_sd: np.ndarray | None       # [H, SI] bf16 bits
+    attempts: np.ndarray = field(default=None)
+
+
+def make_latent_inputs(cfg: LatentConfig, seed: int = 0, attempts: np.ndarray | None = None,
+                       use_stored_attempts: bool = True) -> LatentInputs:
+    """All inputs of one latent layer.  x, w_gate, bias and the Zipf offset are
+    the routing workload's (cfg.router()); the experts' tensors those of
+    cfg.block(); dense weights ~ N(0, 1/fan-in) in bf16, ln_w ~ U(0.5, 1.5)."""
+    r, b = cfg.router(), cfg.block()
+    if attempts is None and use_stored_attempts:
+        attempts = stored_attempts(r, seed)
+    if attempts is None:
+        attempts = np.zeros(cfg.S, np.int64)
+    H, LAT, SI = cfg.H, cfg.LAT, cfg.SI
+    ln_u = uniform01(draws(stream_key(seed, T_LN_W), 0, LAT))
+    return LatentInputs(
+        cfg=cfg, seed=seed,
+        x=gen_x(r, seed, attempts), w_gate=gen_w_gate(r, seed), bias=gen_bias(r, seed),
+        logit_off=gen_logit_offset(r, seed),
+        w_ld=_normal_bf16(stream_key(seed, T_W_LD), LAT * H, 1.0 / math.sqrt(H)).reshape(LAT, H),
+        w13=gen_w13(b, seed), w13s=gen_w13s(b, seed), w2=gen_w2(b, seed), w2s=gen_w2s(b, seed),
+        ln_w=(0.5 + ln_u).astype(np.float32),
+        w_up=_normal_bf16(stream_key(seed, T_W_UP), H * LAT, 1.0 / math.sqrt(LAT)).reshape(H, LAT),
+        w_sgu=_normal_bf16(stream_key(seed, T_W_SGU), 2 * SI * H, 1.0 / math.sqrt(H)).reshape(2 * SI, H)
+        if SI else None,
+        w_sd=_normal_bf16(stream_key(seed, T_W_SD), H * SI, 1.0 / math.sqrt(SI)).reshape(H, SI) if SI else None,
+        attempts=np.asarray(attempts, np.int64),
+    )
+
+
+def latent_dense_bytes(cfg: LatentConfig) -> int:
+    """Bytes of the layer's dense bf16 weights: router, latent down, up and the
+    shared expert."""
+    return 2 * (cfg.E * cfg.H + 2 * cfg.LAT * cfg.H + 3 * cfg.SI * cfg.H)

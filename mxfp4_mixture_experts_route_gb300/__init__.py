@@ -32,7 +32,7 @@ MOE_LOGIT_OFFSET = 2
 EXPORTS = ("moe_abi_version", "moe_strerror", "moe_workspace_bytes", "moe_workspace_init",
            "moe_route", "moe_experts", "moe_forward", "moe_forward_host", "moe_device_status",
            "moe_timing_enable", "moe_timing_collect", "moe_kernel_name", "moe_forward_noalloc",
-           "moe_workspace_region")
+           "moe_workspace_region", "moe_latent_workspace_bytes", "moe_latent_forward")
 
 # workspace regions (moe_workspace_region)
 MOE_WS_STATUS, MOE_WS_POS, MOE_WS_TILES, MOE_WS_XQ, MOE_WS_XS, MOE_WS_HQ, MOE_WS_HS, MOE_WS_Y = range(8)
@@ -47,6 +47,17 @@ class MoEShape(ctypes.Structure):
     def of(cls, S, d, E, k, I, post_norm=False, logit_offset=False, norm_eps=1e-6):
         flags = (MOE_POST_NORM if post_norm else 0) | (MOE_LOGIT_OFFSET if logit_offset else 0)
         return cls(S, d, E, k, I, flags, norm_eps)
+
+
+class LatentShape(ctypes.Structure):
+    """moe_latent_shape: the latent-MoE layer around the routed block."""
+    _fields_ = [("S", ctypes.c_int32), ("H", ctypes.c_int32), ("LAT", ctypes.c_int32),
+                ("E", ctypes.c_int32), ("k", ctypes.c_int32), ("I", ctypes.c_int32),
+                ("SI", ctypes.c_int32), ("flags", ctypes.c_uint32), ("norm_eps", ctypes.c_float)]
+
+    @classmethod
+    def of(cls, S, H, LAT, E, k, I, SI, logit_offset=False, norm_eps=1e-6):
+        return cls(S, H, LAT, E, k, I, SI, MOE_LOGIT_OFFSET if logit_offset else 0, norm_eps)
 
 
 class MoEError(RuntimeError):
@@ -92,6 +103,9 @@ def load_library(path: str) -> ctypes.CDLL:
     L.moe_forward_noalloc.argtypes = [_SP] + [_P] * 14
     L.moe_workspace_region.argtypes = [_SP, ctypes.c_int, ctypes.POINTER(ctypes.c_size_t),
                                        ctypes.POINTER(ctypes.c_size_t)]
+    _LSP = ctypes.POINTER(LatentShape)
+    L.moe_latent_workspace_bytes.argtypes = [_LSP, ctypes.POINTER(ctypes.c_size_t)]
+    L.moe_latent_forward.argtypes = [_LSP] + [_P] * 17 + [ctypes.c_size_t, _P]
     L.moe_timing_enable.argtypes = [ctypes.c_int]
     L.moe_timing_collect.argtypes = [_P, _P, ctypes.c_int, ctypes.POINTER(ctypes.c_int)]
     L.moe_kernel_name.argtypes = [ctypes.c_int]
@@ -189,6 +203,20 @@ def forward_host(shape, x_host, w_gate, bias, logit_off, w13, w13s, w2, w2s, nor
                                   _ptr(ws), ws.numel(), _stream(stream)), "moe_forward_host")
 
 
+def latent_workspace_bytes(shape: LatentShape) -> int:
+    n = ctypes.c_size_t(0)
+    _check(lib().moe_latent_workspace_bytes(ctypes.byref(shape), ctypes.byref(n)), "moe_latent_workspace_bytes")
+    return n.value
+
+
+def latent_forward(shape, x, w_gate, bias, logit_off, w_ld, w13, w13s, w2, w2s, ln_w, w_up, w_sgu, w_sd,
+                   ids, weights, out, ws, stream=None) -> None:
+    _check(lib().moe_latent_forward(ctypes.byref(shape), _ptr(x), _ptr(w_gate), _ptr(bias), _ptr(logit_off),
+                                    _ptr(w_ld), _ptr(w13), _ptr(w13s), _ptr(w2), _ptr(w2s), _ptr(ln_w),
+                                    _ptr(w_up), _ptr(w_sgu), _ptr(w_sd), _ptr(ids), _ptr(weights), _ptr(out),
+                                    _ptr(ws), ws.numel(), _stream(stream)), "moe_latent_forward")
+
+
 def device_status(ws, stream=None) -> tuple[int, int]:
     """(status, detail) latched on the device since the last call; clears it."""
     det = ctypes.c_int32(0)
@@ -257,4 +285,44 @@ class DeviceWeights:
         forward(self.shape, self.x if x is None else x, self.w_gate, self.bias, self.logit_off,
                 self.w13, self.w13s, self.w2, self.w2s, self.norm_w, self.ids, self.weights,
                 self.out, self.ws, stream)
+        return self.ids, self.weights, self.out
+
+
+class DeviceLatentWeights:
+    """Device copies of one latent-MoE layer's weights and step input (host
+    arrays: bf16 bit patterns as uint16, packed e2m1 / e8m0 as uint8, fp32)."""
+
+    def __init__(self, shape: LatentShape, x, w_gate, bias, logit_off, w_ld, w13, w13s, w2, w2s, ln_w,
+                 w_up, w_sgu, w_sd, device="cuda"):
+        import torch
+
+        def up(a, dtype=None):
+            if a is None:
+                return None
+            t = torch.as_tensor(a)
+            if dtype is not None:
+                t = t.view(dtype)
+            return t.contiguous().to(device)
+
+        bf = torch.bfloat16
+        self.shape = shape
+        self.x = up(x, bf)
+        self.w_gate, self.bias, self.logit_off = up(w_gate, bf), up(bias), up(logit_off)
+        self.w_ld, self.w_up, self.ln_w = up(w_ld, bf), up(w_up, bf), up(ln_w)
+        self.w13, self.w13s, self.w2, self.w2s = up(w13), up(w13s), up(w2), up(w2s)
+        self.w_sgu, self.w_sd = up(w_sgu, bf), up(w_sd, bf)
+        S, k, H = shape.S, shape.k, shape.H
+        self.ids = torch.empty((S, k), dtype=torch.int32, device=device)
+        self.weights = torch.empty((S, k), dtype=torch.float32, device=device)
+        self.out = torch.empty((S, H), dtype=torch.float32, device=device)
+        nbytes = latent_workspace_bytes(shape)
+        buf = torch.empty(nbytes + 256, dtype=torch.uint8, device=device)
+        off = (-buf.data_ptr()) % 256
+        self.ws = buf[off:off + nbytes]
+        _check(lib().moe_workspace_init(self.ws.data_ptr(), nbytes, _stream(None)), "moe_workspace_init")
+
+    def forward(self, x=None, stream=None):
+        latent_forward(self.shape, self.x if x is None else x, self.w_gate, self.bias, self.logit_off, self.w_ld,
+                       self.w13, self.w13s, self.w2, self.w2s, self.ln_w, self.w_up, self.w_sgu, self.w_sd,
+                       self.ids, self.weights, self.out, self.ws, stream)
         return self.ids, self.weights, self.out

@@ -285,6 +285,40 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate, const
 }  // extern "C"
 
 namespace {
+// The latent layer's workspace: the block's workspace for the larger of its
+// two shapes (the router over H, the experts over LAT; the two calls run one
+// after the other on the stream, so they share it), then the layer's own
+// activations.
+struct LatentLayout {
+    moe_shape sr, sx;      // routing over H; experts over LAT
+    WsLayout Lr, Lx;
+    size_t xl, yl, zl, gu, hs, total;
+};
+
+int latent_layout(const moe_latent_shape* ls, LatentLayout& o) {
+    if (!ls) return MOE_ERR_INVALID_ARG;
+    if (ls->flags & ~MOE_LOGIT_OFFSET) return MOE_ERR_INVALID_ARG;
+    if (ls->SI < 0 || ls->H < 1 || ls->LAT < 1) return MOE_ERR_INVALID_ARG;
+    if (ls->SI % 128 || ls->SI > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+    o.sr = moe_shape{ls->S, ls->H, ls->E, ls->k, ls->I, ls->flags, ls->norm_eps};
+    o.sx = moe_shape{ls->S, ls->LAT, ls->E, ls->k, ls->I, 0u, ls->norm_eps};
+    int rc = check_shape(&o.sr);
+    if (!rc) rc = check_shape(&o.sx);
+    if (rc) return rc;
+    o.Lr = ws_layout(o.sr);
+    o.Lx = ws_layout(o.sx);
+    size_t at = align256(o.Lr.total > o.Lx.total ? o.Lr.total : o.Lx.total);
+    auto take = [&](size_t bytes) { size_t r = at; at = align256(at + bytes); return r; };
+    const size_t S = (size_t)ls->S;
+    o.xl = take(S * ls->LAT * 2);
+    o.yl = take(S * ls->LAT * 4);
+    o.zl = take(S * ls->LAT * 2);
+    o.gu = take(S * 2 * (size_t)ls->SI * 4);
+    o.hs = take(S * (size_t)ls->SI * 2);
+    o.total = at;
+    return MOE_OK;
+}
+
 // The device address of a 16-byte aligned pinned host buffer the GPU reads and
 // writes in place (cudaHostAlloc'd or registered memory under unified
 // addressing; on GB300 over the coherent CPU-GPU link), else nullptr: pageable
@@ -351,6 +385,94 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
         rc = cuda_rc(cudaMemcpyAsync(ids_host, ids_dev, P * 4, cudaMemcpyDeviceToHost, st));
     if (!rc && weights_host && wts_staged)
         rc = cuda_rc(cudaMemcpyAsync(weights_host, wts_dev, P * 4, cudaMemcpyDeviceToHost, st));
+    return rc;
+}
+
+int moe_latent_workspace_bytes(const moe_latent_shape* shape, size_t* bytes) {
+    LatentLayout LL;
+    const int rc = latent_layout(shape, LL);
+    if (rc) return rc;
+    if (!bytes) return MOE_ERR_INVALID_ARG;
+    *bytes = LL.total;
+    return MOE_OK;
+}
+
+int moe_latent_forward(const moe_latent_shape* shape, const void* x, const void* w_gate, const float* bias,
+                       const float* logit_off, const void* w_ld, const uint8_t* w13, const uint8_t* w13s,
+                       const uint8_t* w2, const uint8_t* w2s, const float* ln_w, const void* w_up, const void* w_sgu,
+                       const void* w_sd, int32_t* ids, float* weights, float* out, void* ws, size_t ws_bytes,
+                       void* stream) {
+    LatentLayout LL;
+    int rc = latent_layout(shape, LL);
+    if (rc) return rc;
+    const moe_latent_shape& ls = *shape;
+    const bool shared = ls.SI > 0;
+    if (!x || !w_gate || !bias || !w_ld || !w13 || !w13s || !w2 || !w2s || !ln_w || !w_up || !ids || !weights || !out)
+        return MOE_ERR_INVALID_ARG;
+    if ((ls.flags & MOE_LOGIT_OFFSET) && !logit_off) return MOE_ERR_INVALID_ARG;
+    if (shared && (!w_sgu || !w_sd)) return MOE_ERR_INVALID_ARG;
+    if (!a16(x) || !a16(w_gate) || !a16(bias) || !a16(w_ld) || !a32(w13) || !a16(w13s) || !a32(w2) || !a16(w2s) ||
+        !a16(ln_w) || !a16(w_up) || !a16(ids) || !a16(weights) || !a16(out))
+        return MOE_ERR_ALIGNMENT;
+    if ((ls.flags & MOE_LOGIT_OFFSET) && !a16(logit_off)) return MOE_ERR_ALIGNMENT;
+    if (shared && (!a16(w_sgu) || !a16(w_sd))) return MOE_ERR_ALIGNMENT;
+    if (!ws) return MOE_ERR_INVALID_ARG;
+    if ((uintptr_t)ws & 255) return MOE_ERR_ALIGNMENT;
+    if (ws_bytes < LL.total) return MOE_ERR_WORKSPACE;
+    rc = check_device();
+    if (rc) return rc;
+    cudaStream_t st = (cudaStream_t)stream;
+    char* w = (char*)ws;
+    StatusBlock* sb = reinterpret_cast<StatusBlock*>(w + LL.Lr.status);
+    const int S = ls.S;
+    // route over the layer input (k2 page: the router parts read x)
+    Ptrs pr{};
+    pr.x = (const __nv_bfloat16*)x;
+    pr.w_gate = (const __nv_bfloat16*)w_gate;
+    pr.bias = bias;
+    pr.logit_off = (ls.flags & MOE_LOGIT_OFFSET) ? logit_off : nullptr;
+    pr.ids = ids;
+    pr.weights = weights;
+    pr.ws = w;
+    rc = run_route(LL.sr, LL.Lr, pr, st);
+    // latent parts: xl = x . w_ld^T (bf16)
+    auto dense = [&](int kid, const void* in, const void* wt, int K, int N, void* o, int mode) {
+        if (rc) return;
+        timing_begin(kid, st);
+        rc = cuda_rc(launch_dense(in, wt, S, K, N, nullptr, o, mode, sb, st));
+        timing_end(st);
+    };
+    dense(K_LATENT_DOWN, x, w_ld, ls.H, ls.LAT, w + LL.xl, DENSE_BF16);
+    // the routed block on the latent rows
+    if (!rc) {
+        Ptrs px{};
+        px.x = (const __nv_bfloat16*)(w + LL.xl);
+        px.ids = ids;
+        px.weights = weights;
+        px.w13 = w13; px.w13s = w13s; px.w2 = w2; px.w2s = w2s;
+        px.norm_w = nullptr;
+        px.out = (float*)(w + LL.yl);
+        px.ws = w;
+        rc = run_experts(LL.sx, LL.Lx, px, st);
+    }
+    // lnorm, up
+    if (!rc) {
+        timing_begin(K_LATENT_NORM, st);
+        rc = cuda_rc(launch_latent_norm((const float*)(w + LL.yl), ln_w, ls.norm_eps, S, ls.LAT,
+                                        (__nv_bfloat16*)(w + LL.zl), st));
+        timing_end(st);
+    }
+    dense(K_LATENT_UP, w + LL.zl, w_up, ls.LAT, ls.H, out, DENSE_F32);
+    // the shared expert on the layer input, added to the output
+    if (shared) {
+        dense(K_SHARED_GU, x, w_sgu, ls.H, 2 * ls.SI, w + LL.gu, DENSE_F32);
+        if (!rc) {
+            timing_begin(K_SHARED_ACT, st);
+            rc = cuda_rc(launch_shared_act((const float*)(w + LL.gu), S, ls.SI, (__nv_bfloat16*)(w + LL.hs), st));
+            timing_end(st);
+        }
+        dense(K_SHARED_DOWN, w + LL.hs, w_sd, ls.SI, ls.H, out, DENSE_F32_ADD);
+    }
     return rc;
 }
 

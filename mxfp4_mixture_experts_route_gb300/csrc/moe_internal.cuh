@@ -120,7 +120,8 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // per-kernel timing hooks (moe_timing_*): no-ops unless enabled
 // ---------------------------------------------------------------------------
 enum KernelId {
-    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_TOPK_SORT, K_NUM
+    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_TOPK_SORT,
+    K_LATENT_DOWN, K_LATENT_NORM, K_LATENT_UP, K_SHARED_GU, K_SHARED_ACT, K_SHARED_DOWN, K_NUM
 };
 void timing_begin(int kernel_id, cudaStream_t st);
 void timing_end(cudaStream_t st);
@@ -148,6 +149,13 @@ cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Pt
 // the router's tensor-core kernel (S >= 64, E a multiple of 128)
 bool router_tc_fits(const moe_shape& s);
 cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+// dense bf16 product out[S, N] = x[S, K] . w[N, K]^T on the tensor cores
+// (route_tc.cu): N % 128 == 0, K % 64 == 0; out fp32 (store, or add to what
+// the stream's earlier kernels wrote) or bf16
+enum DenseOut { DENSE_F32 = 0, DENSE_F32_ADD = 1, DENSE_BF16 = 2 };
+bool dense_fits(int S, int K, int N);
+cudaError_t launch_dense(const void* x, const void* w, int S, int K, int N, const float* off, void* out, int mode,
+                         StatusBlock* sb, cudaStream_t st);
 cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 // moe_forward at small S: top-k and sort in one kernel (needs the logits)
 bool topk_sort_fits(const moe_shape& s);
@@ -155,5 +163,9 @@ cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+// the latent-MoE layer's elementwise steps (latent.cu)
+cudaError_t launch_latent_norm(const float* yl, const float* ln_w, float eps, int S, int n, __nv_bfloat16* zl,
+                               cudaStream_t st);
+cudaError_t launch_shared_act(const float* gu, int S, int si, __nv_bfloat16* hs, cudaStream_t st);
 
 }  // namespace moe

@@ -1,4 +1,6 @@
-// Router logits on the tensor cores, for batches of 64 tokens and more.
+// Dense bf16 products on the tensor cores: the router's logits for batches of
+// 64 tokens and more, and the latent-MoE layer's dense projections (latent
+// down and up, the shared expert), at any batch.
 //
 // vllm.models.muse_spark.amd.mono.kernels.k3, stage A (the router's logits in
 // fp32); the pages split the router's K over 8-CTA groups.  At larger batches the
@@ -24,23 +26,40 @@ namespace moe {
 
 namespace {
 
-constexpr int RM = 128;                    // experts per tile (MMA M)
-constexpr int RN = 128;                    // tokens per tile (MMA N)
+constexpr int RM = 128;                    // weight rows per tile (MMA M)
 constexpr int RK = 64;                     // K elements per stage (one 128-byte slab)
-constexpr int RS = 6;                      // stages
-constexpr int R_A = RM * RK * 2;           // 16 KB
-constexpr int R_B = RN * RK * 2;           // 16 KB
-constexpr int R_STAGE = R_A + R_B;
+constexpr int R_A = RM * RK * 2;           // 16 KB of weights a stage
 constexpr int R_THREADS = 192;
 constexpr int R_MAX_CLUSTER = 8;
-constexpr int R_SMEM = 1024 + RS * R_STAGE + 256;
 constexpr uint64_t R_WAIT_NS = 2000000000ull;
-static_assert(RS * R_STAGE >= RM * RN * 4, "the partial tile reuses the stage ring");
 
+// RN: token rows a tile (the MMA N): 128 for batches, 16 for a few tokens,
+// where a 2 KB token slab a stage leaves room for twice the weight stages
+// (the weight stream is the cost of a small-batch product).
+template <int RN>
+struct DCfg {
+    static constexpr int R_B = RN * RK * 2;
+    static constexpr int R_STAGE = R_A + R_B;
+    static constexpr int RS_FIT = (232448 - 1024 - 256) / R_STAGE;
+    static constexpr int RS = RS_FIT < 12 ? RS_FIT : 12;
+    static constexpr int SMEM = 1024 + RS * R_STAGE + 256;
+    static constexpr int TMEM_COLS = RN < 32 ? 32 : RN;
+    static_assert(RS >= 4 && SMEM <= 232448, "stages");
+    static_assert(RS * R_STAGE >= RM * RN * 4, "the partial tile reuses the stage ring");
+};
+
+// out[t, n] = sum_k x[t, k] * w[n, k]: x [S, K] bf16, w [N, K] bf16, fp32
+// accumulation in TMEM.  grid (N / 128, ceil(S / RN), kslices) in clusters of
+// (1, 1, kslices) over K.  The weight slabs of the first stages are issued
+// before the wait on the preceding kernel (the weights are inputs of the
+// call); the token slabs after it.
+template <int RN>
 __global__ void __launch_bounds__(R_THREADS, 1)
-    k_router_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
-                const float* __restrict__ off, float* __restrict__ L, int S, int d, int E, int kslices,
-                StatusBlock* __restrict__ sb) {
+    k_dense_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+               const float* __restrict__ off, void* out, int S, int K, int N, int kslices, int mode,
+               int w_evict_first, StatusBlock* __restrict__ sb) {
+    using C = DCfg<RN>;
+    constexpr int RS = C::RS, R_STAGE = C::R_STAGE;
     extern __shared__ uint8_t smem_raw[];
     uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint64_t* full = reinterpret_cast<uint64_t*>(sm + RS * R_STAGE);
@@ -48,11 +67,11 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     uint64_t* done = empty + RS;
     uint32_t* holder = reinterpret_cast<uint32_t*>(done + 1);
     volatile int* abort_flag = reinterpret_cast<volatile int*>(holder + 1);
-    float* part = reinterpret_cast<float*>(sm);   // [RN][RM] partial logits, after the MMAs
+    float* part = reinterpret_cast<float*>(sm);   // [RN][RM] partial products, after the MMAs
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e0 = blockIdx.x * RM, t0 = blockIdx.y * RN, ks = blockIdx.z;
-    const int nk = d / RK;
+    const int nk = K / RK;
     const int kb = (int)((long long)nk * ks / kslices), ke = (int)((long long)nk * (ks + 1) / kslices);
     if (threadIdx.x == 0) {
         for (int i = 0; i < RS; ++i) {
@@ -63,7 +82,9 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         *abort_flag = 0;
         ptx::fence_mbar_init();
     }
-    if (warp == 1) ptx::tmem_alloc(holder, RN);
+    if (warp == 1) ptx::tmem_alloc(holder, C::TMEM_COLS);
+    const uint64_t pol_w = w_evict_first ? ptx::policy_evict_first() : ptx::policy_evict_last();
+    const uint64_t pol_x = ptx::policy_evict_last();
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tm_w);
         ptx::prefetch_tensormap(&tm_x);
@@ -72,8 +93,15 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *holder;
+    const int n_pre = ke - kb < RS ? ke - kb : RS;   // stages whose weights go out before the wait
+    if (warp == 0 && lane == 0) {
+        for (int i = 0; i < n_pre; ++i) {
+            ptx::mbar_arrive_expect_tx(&full[i], R_STAGE);
+            ptx::tma_load_2d(sm + i * R_STAGE, &tm_w, (kb + i) * RK, e0, &full[i], pol_w);
+        }
+    }
     pdl_wait();      // x may come from the stream's previous kernel
-    pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
+    pdl_trigger();   // successors start once this kernel's inputs are final
 
     auto fail = [&](int site) {
         latch_status(sb, MOE_ERR_TIMEOUT, 100 + site);
@@ -81,17 +109,18 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     };
     if (warp == 0) {
         if (lane == 0) {
-            const uint64_t pol = ptx::policy_evict_last();   // w_gate is read by every token tile
             for (int k = kb, i = 0; k < ke; ++k, ++i) {
                 const int s = i % RS;
-                if (i >= RS && !ptx::mbar_wait(&empty[s], ((i / RS) & 1) ^ 1, abort_flag, R_WAIT_NS)) {
-                    fail(1);
-                    break;
-                }
                 uint8_t* st = sm + s * R_STAGE;
-                ptx::mbar_arrive_expect_tx(&full[s], R_STAGE);
-                ptx::tma_load_2d(st, &tm_w, k * RK, e0, &full[s], pol);
-                ptx::tma_load_2d(st + R_A, &tm_x, k * RK, t0, &full[s], pol);
+                if (i >= n_pre) {
+                    if (!ptx::mbar_wait(&empty[s], ((i / RS) & 1) ^ 1, abort_flag, R_WAIT_NS)) {
+                        fail(1);
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[s], R_STAGE);
+                    ptx::tma_load_2d(st, &tm_w, k * RK, e0, &full[s], pol_w);
+                }
+                ptx::tma_load_2d(st + R_A, &tm_x, k * RK, t0, &full[s], pol_x);
             }
         }
     } else if (warp == 1) {
@@ -114,7 +143,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
             ptx::mma_commit(done);   // arrives once every MMA above has completed
         }
     } else {
-        // epilogue: row m = 32 (warp mod 4) + lane of the tile, 128 token columns
+        // epilogue: row m = 32 (warp mod 4) + lane of the tile, RN token columns
         const int q = warp & 3;
         const int m = 32 * q + lane;
         const bool got = ptx::mbar_wait_warp(done, 0, abort_flag, R_WAIT_NS);
@@ -149,39 +178,47 @@ __global__ void __launch_bounds__(R_THREADS, 1)
 #pragma unroll
             for (int r = 0; r < R_MAX_CLUSTER; ++r) z += pz[r];
             const int t = t0 + n, e = e0 + mm;
-            if (t < S && e < E) L[(size_t)t * E + e] = off ? z + off[e] : z;
+            if (t < S && e < N) {
+                const size_t o = (size_t)t * N + e;
+                if (mode == DENSE_BF16) {
+                    reinterpret_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(z);
+                } else if (mode == DENSE_F32_ADD) {
+                    float* of = reinterpret_cast<float*>(out);
+                    of[o] = ld_dep(of + o) + z;
+                } else {
+                    reinterpret_cast<float*>(out)[o] = off ? z + off[e] : z;
+                }
+            }
         }
     }
     cluster.sync();   // every CTA keeps its partial tile until the others have read it
     ptx::tc_fence_after();
-    if (warp == 1) ptx::tmem_dealloc(tmem, RN);
+    if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-}  // namespace
-
-bool router_tc_fits(const moe_shape& s) { return s.S >= 64 && s.E % RM == 0 && s.d % RK == 0; }
-
-cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+template <int RN>
+cudaError_t launch_dense_rn(const void* x, const void* w, int S, int K, int N, const float* off, void* out,
+                            int mode, bool w_once, StatusBlock* sb, cudaStream_t st) {
+    using C = DCfg<RN>;
     CUtensorMap tm_w, tm_x;
-    const uint64_t d = s.d, E = s.E, S = s.S;
-    const uint64_t w_d[2] = {d, E}, w_s[1] = {d * 2};
-    const uint64_t x_d[2] = {d, S}, x_s[1] = {d * 2};
+    const uint64_t w_d[2] = {(uint64_t)K, (uint64_t)N}, w_s[1] = {(uint64_t)K * 2};
+    const uint64_t x_d[2] = {(uint64_t)K, (uint64_t)S}, x_s[1] = {(uint64_t)K * 2};
     const uint32_t w_b[2] = {RK, RM}, x_b[2] = {RK, RN};
-    if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.w_gate, 2, w_d, w_s, w_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, p.x, 2, x_d, x_s, x_b, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, 2, w_d, w_s, w_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, x_d, x_s, x_b, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const int tiles = (s.E / RM) * ((s.S + RN - 1) / RN);
-    const int nk = s.d / RK;
+    const int tiles = (N / RM) * ((S + RN - 1) / RN);
+    const int nk = K / RK;
     int ks = (num_sms() + tiles - 1) / tiles;   // about one CTA per SM
     if (ks > R_MAX_CLUSTER) ks = R_MAX_CLUSTER;
     if (ks > nk / 4) ks = nk / 4;               // at least four slabs per CTA
     if (ks < 1) ks = 1;
-    cudaError_t e = cudaFuncSetAttribute(k_router_tc, cudaFuncAttributeMaxDynamicSharedMemorySize, R_SMEM);
+    cudaError_t e = cudaFuncSetAttribute(k_dense_tc<RN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(s.E / RM, (s.S + RN - 1) / RN, ks);
+    cfg.gridDim = dim3(N / RM, (S + RN - 1) / RN, ks);
     cfg.blockDim = dim3(R_THREADS);
-    cfg.dynamicSmemBytes = R_SMEM;
+    cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
     cudaLaunchAttribute attr[2];
     attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -192,8 +229,26 @@ cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& 
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_router_tc, tm_w, tm_x, p.logit_off, reinterpret_cast<float*>(p.ws + L.logits),
-                              s.S, s.d, s.E, ks, reinterpret_cast<StatusBlock*>(p.ws + L.status));
+    return cudaLaunchKernelEx(&cfg, k_dense_tc<RN>, tm_w, tm_x, off, out, S, K, N, ks, mode, w_once ? 1 : 0, sb);
+}
+
+}  // namespace
+
+bool router_tc_fits(const moe_shape& s) { return s.S >= 64 && s.E % RM == 0 && s.d % RK == 0; }
+
+bool dense_fits(int S, int K, int N) { return S >= 1 && N % RM == 0 && K % RK == 0 && K / RK >= 1; }
+
+cudaError_t launch_dense(const void* x, const void* w, int S, int K, int N, const float* off, void* out, int mode,
+                         StatusBlock* sb, cudaStream_t st) {
+    // one token tile of 16 for up to 16 tokens (a weight-streaming product), else tiles of 128; the
+    // weights are read once (evict first) unless several token tiles read them
+    if (S <= 16) return launch_dense_rn<16>(x, w, S, K, N, off, out, mode, true, sb, st);
+    return launch_dense_rn<128>(x, w, S, K, N, off, out, mode, S <= 128, sb, st);
+}
+
+cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    return launch_dense_rn<128>(p.x, p.w_gate, s.S, s.d, s.E, p.logit_off, p.ws + L.logits, DENSE_F32, false,
+                                reinterpret_cast<StatusBlock*>(p.ws + L.status), st);
 }
 
 }  // namespace moe

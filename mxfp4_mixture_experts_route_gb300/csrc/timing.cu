@@ -17,7 +17,9 @@ std::vector<Rec> g_recs;   // event pairs, created by moe_timing_enable
 int g_used = 0;            // pairs recorded since the last collect
 int g_open = -1;           // pair started by timing_begin, not yet ended
 
-const char* const kNames[K_NUM] = {"router_logits", "topk", "sort", "gather", "experts", "combine", "topk_sort"};
+const char* const kNames[K_NUM] = {"router_logits", "topk", "sort", "gather", "experts", "combine", "topk_sort",
+                                   "latent_down", "latent_norm", "latent_up", "shared_gate_up", "shared_act",
+                                   "shared_down"};
 
 void free_all() {
     for (auto& r : g_recs) {

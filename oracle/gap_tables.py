@@ -47,7 +47,7 @@ def enforce_gap(cfg: mi.MoEConfig, seed: int = 0) -> np.ndarray:
 def main() -> None:
     path = os.path.join(os.path.dirname(os.path.abspath(mi.__file__)), "gap_attempts.json")
     tab = {}
-    for cfg in mi.CONFIGS:
+    for cfg in list(mi.CONFIGS) + [lc.router() for lc in mi.LATENT_CONFIGS]:
         att = enforce_gap(cfg, 0)
         rows = np.nonzero(att)[0]
         tab[f"{cfg.name}/seed0"] = {

@@ -225,6 +225,51 @@ def moe_forward(inp, tokens: np.ndarray | None = None):
     return ids, w, out, L
 
 
+# ----------------------------------------------------------------------------
+# the latent-MoE layer around the block (k2 page, K2b: router parts, latent
+# parts, route, ug / down, lnorm, up; shared gate/up, its activation, shared
+# down; k2_launch w_gate, bias, w_ld, w_sgu, w_sd, w13, w13s, w2, w2s, ln_w,
+# w_up, out [S, 7168])
+# ----------------------------------------------------------------------------
+
+
+def dense(xf: np.ndarray, w_bits: np.ndarray) -> np.ndarray:
+    """x [n, K] (fp64) times a bf16 weight [N, K] transposed: [n, N]."""
+    return xf @ bf16_to_f64(w_bits).T
+
+
+def shared_expert(xf: np.ndarray, w_sgu: np.ndarray, w_sd: np.ndarray) -> np.ndarray:
+    """The shared expert on rows xf [n, H]: (silu(x Wg^T) * (x Wu^T)) Wd^T, with
+    w_sgu = [Wg; Wu] (gate rows first, as w13) and w_sd = Wd [H, SI]."""
+    SI = w_sgu.shape[0] // 2
+    gu = dense(xf, w_sgu)
+    return dense(silu(gu[:, :SI]) * gu[:, SI:], w_sd)
+
+
+def latent_forward(inp, tokens: np.ndarray | None = None):
+    """The latent-MoE layer on a ``moe_inputs.LatentInputs``, in fp64 (fp32
+    logits).  Returns (ids, w, out [n, H], logits) for the rows ``tokens``.
+
+      routing  on x (the router parts read the layer input)
+      xl       = x . w_ld^T                       (latent parts)
+      yl       = sum_j w_j expert_j(xl)            (ug, down: the block at d = LAT)
+      zl       = RMSNorm(yl) * ln_w                (lnorm)
+      out      = zl . w_up^T + shared_expert(x)   (up; shared gate/up, down)"""
+    cfg = inp.cfg
+    rows = np.arange(cfg.S) if tokens is None else np.asarray(tokens)
+    xb = inp.x[rows]
+    L = router_logits(xb, inp.w_gate, inp.logit_off)
+    ids, w = route(L, inp.bias, cfg.k)
+    xf = bf16_to_f64(xb)
+    xl = dense(xf, inp.w_ld)
+    yl = experts_combine(xl, ids, w, inp.w13, inp.w13s, inp.w2, inp.w2s)
+    zl = post_expert_norm(yl, inp.ln_w, cfg.norm_eps)
+    out = dense(zl, inp.w_up)
+    if cfg.SI:
+        out = out + shared_expert(xf, inp.w_sgu, inp.w_sd)
+    return ids, w, out, L
+
+
 def parity_error(out_gpu: np.ndarray, out_ref: np.ndarray) -> float:
     """max |out - ref| / max |ref| -- the output parity measure."""
     ref = np.asarray(out_ref, np.float64)

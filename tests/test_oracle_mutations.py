@@ -103,3 +103,59 @@ def test_pins_catch_mutation(name, monkeypatch):
         except AssertionError:
             failed.append(getattr(pin, "__name__", "brute"))
     assert failed, f"no pin caught the planted mistake '{name}' in {orig.__name__}"
+
+
+# ---------------------------------------------------------------------------
+# the latent-MoE layer (tests/test_oracle_latent.py's pins)
+# ---------------------------------------------------------------------------
+import test_oracle_latent as TL  # noqa: E402
+
+_ORIG_L = {n: getattr(M, n) for n in ("dense", "shared_expert")}
+
+
+def _shared_gate_up_swapped(xf, w_sgu, w_sd):
+    SI = w_sgu.shape[0] // 2
+    gu = _ORIG_L["dense"](xf, w_sgu)
+    return _ORIG_L["dense"](M.silu(gu[:, SI:]) * gu[:, :SI], w_sd)
+
+
+def _shared_sigmoid(xf, w_sgu, w_sd):
+    SI = w_sgu.shape[0] // 2
+    gu = _ORIG_L["dense"](xf, w_sgu)
+    return _ORIG_L["dense"](M.sigmoid(gu[:, :SI]) * gu[:, SI:], w_sd)
+
+
+def _shared_dropped(xf, w_sgu, w_sd):
+    return np.zeros((xf.shape[0], w_sd.shape[0]))
+
+
+def _dense_square_transposed(xf, w_bits):
+    W = M.bf16_to_f64(w_bits)
+    return xf @ W if W.shape[0] == W.shape[1] else xf @ W.T
+
+
+LATENT_MUTATIONS = {
+    "shared gate/up swapped": ("shared_expert", _shared_gate_up_swapped),
+    "shared activation sigmoid": ("shared_expert", _shared_sigmoid),
+    "shared expert dropped": ("shared_expert", _shared_dropped),
+    "projection not transposed": ("dense", _dense_square_transposed),
+    "latent norm weight dropped": ("post_expert_norm", _norm_without_weight),
+}
+
+LATENT_PINS = [lambda c=c: TL.test_latent_brute_force_tiny(c) for c in TL.BRUTE] + [
+    TL.test_permutation_projections_reduce_to_the_block, TL.test_shared_expert_with_zero_gate_adds_nothing,
+]
+
+
+@pytest.mark.parametrize("name", sorted(LATENT_MUTATIONS))
+def test_latent_pins_catch_mutation(name, monkeypatch):
+    fname, fake = LATENT_MUTATIONS[name]
+    monkeypatch.setattr(M, fname, fake)
+    monkeypatch.setattr(oracle, fname, fake)
+    failed = 0
+    for pin in LATENT_PINS:
+        try:
+            pin()
+        except AssertionError:
+            failed += 1
+    assert failed, f"no latent pin caught the planted mistake '{name}'"
