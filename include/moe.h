@@ -330,6 +330,7 @@ int moe_device_status(void* ws, int32_t* detail, void* stream);
  *                  block b of position r at [b / 8][r][b % 8]
  *   MOE_WS_HQ, MOE_WS_HS  the same for h = silu(g) * u (K = I)
  *   MOE_WS_Y       fp32 [P][d]: expert output of the pick at position r
+ *   MOE_WS_LOGITS  fp32 [S][E]: the router's logits (moe_route, moe_forward)
  */
 #define MOE_WS_STATUS 0
 #define MOE_WS_POS    1
@@ -339,6 +340,7 @@ int moe_device_status(void* ws, int32_t* detail, void* stream);
 #define MOE_WS_HQ     5
 #define MOE_WS_HS     6
 #define MOE_WS_Y      7
+#define MOE_WS_LOGITS 8
 int moe_workspace_region(const moe_shape* shape, int region, size_t* offset, size_t* bytes);
 
 /*

@@ -35,7 +35,7 @@ EXPORTS = ("moe_abi_version", "moe_strerror", "moe_workspace_bytes", "moe_worksp
            "moe_workspace_region", "moe_latent_workspace_bytes", "moe_latent_forward")
 
 # workspace regions (moe_workspace_region)
-MOE_WS_STATUS, MOE_WS_POS, MOE_WS_TILES, MOE_WS_XQ, MOE_WS_XS, MOE_WS_HQ, MOE_WS_HS, MOE_WS_Y = range(8)
+MOE_WS_STATUS, MOE_WS_POS, MOE_WS_TILES, MOE_WS_XQ, MOE_WS_XS, MOE_WS_HQ, MOE_WS_HS, MOE_WS_Y, MOE_WS_LOGITS = range(9)
 
 
 class MoEShape(ctypes.Structure):

@@ -203,6 +203,7 @@ int moe_workspace_region(const moe_shape* shape, int region, size_t* offset, siz
         case MOE_WS_HQ: *offset = L.hq; *bytes = 2 * P * shape->I; break;
         case MOE_WS_HS: *offset = L.hs; *bytes = (size_t)((shape->I + 255) / 256) * rows * TOKEN_SCALE_ROW; break;
         case MOE_WS_Y: *offset = L.y; *bytes = P * shape->d * 4; break;
+        case MOE_WS_LOGITS: *offset = L.logits; *bytes = (size_t)shape->S * shape->E * 4; break;
         default: return MOE_ERR_INVALID_ARG;
     }
     return MOE_OK;

@@ -209,7 +209,7 @@ cudaError_t launch_dense_rn(const void* x, const void* w, int S, int K, int N, c
         return cudaErrorInvalidValue;
     const int tiles = (N / RM) * ((S + RN - 1) / RN);
     const int nk = K / RK;
-    int ks = (num_sms() + tiles - 1) / tiles;   // about one CTA per SM
+    int ks = num_sms() / tiles;                 // at most one CTA per SM: a second wave would double the time
     if (ks > R_MAX_CLUSTER) ks = R_MAX_CLUSTER;
     if (ks > nk / 4) ks = nk / 4;               // at least four slabs per CTA
     if (ks < 1) ks = 1;
