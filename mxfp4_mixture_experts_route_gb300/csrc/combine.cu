@@ -25,8 +25,10 @@ constexpr int CB_MAXK = 16;               // picks per token (k <= 16)
 __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const float* ssq, const int32_t* pos, const float* w,
                                                         const float* __restrict__ norm_w, float eps, int k, int d,
                                                         float* __restrict__ out) {
+    KT_MARK(K_COMBINE, 0);
     pdl_trigger();
     pdl_wait();
+    KT_MARK(K_COMBINE, 1);
     const int t = blockIdx.x;
     __shared__ float coef[CB_MAXK];
     __shared__ int32_t prow[CB_MAXK];
@@ -57,7 +59,10 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const fl
     }
     __syncthreads();
     const int col = blockIdx.y * CB_COLS + 4 * tid;
-    if (col >= d) return;
+    if (col >= d) {
+        KT_MARK(K_COMBINE, 2);
+        return;
+    }
     float4 v[CB_MAXK];
 #pragma unroll
     for (int j = 0; j < CB_MAXK; ++j) {           // every pick's load in flight at once
@@ -83,11 +88,13 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const fl
         acc.w *= nw.w;
     }
     *reinterpret_cast<float4*>(out + (size_t)t * d + col) = acc;
+    KT_MARK(K_COMBINE, 2);
 }
 
 }  // namespace
 
 cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    KT_BIND();
     timing_begin(K_COMBINE, st);
     const dim3 grid(s.S, (s.d + CB_COLS - 1) / CB_COLS);
     const cudaError_t e =

@@ -292,6 +292,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     StatusBlock* sb = a.sb;
     if (threadIdx.x == 0) MOE_TR(TR_MISC, 0);
+    KT_MARK(K_EXPERTS, 0);
     pdl_trigger();
 
     if (threadIdx.x == 0) {
@@ -334,6 +335,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     // below reads their results
     pdl_wait();
     if (threadIdx.x == 0) MOE_TR(TR_MISC, 1);
+    KT_MARK(K_EXPERTS, 1);
     // CTA b's first unit is unit b; the later ones are claimed from the counter
     // (offset by the grid size).  The tile count, the first unit's tile entry
     // (read as if it were a gate_up unit, the usual case, and read again below
@@ -348,6 +350,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     ptx::tc_fence_before();
     __syncthreads();
     ptx::tc_fence_after();
+    KT_MARK(K_EXPERTS, 3);
     const uint32_t tmem = *tmem_holder;
 
     const int mb1 = a.I / 64;
@@ -879,6 +882,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
 
     __syncthreads();
     if (threadIdx.x == 0) MOE_TR(TR_MISC, 2);
+    KT_MARK(K_EXPERTS, 2);
     if (*abort_flag) {
         // let copies still in flight into this CTA's shared memory land
         const uint64_t t0 = ptx::globaltimer();
@@ -993,6 +997,7 @@ int num_sms() {
 }
 
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    KT_BIND();
     timing_begin(K_EXPERTS, st);
     const bool stma = (s.d % 512 == 0) && (s.I % 512 == 0);
     cudaError_t e;

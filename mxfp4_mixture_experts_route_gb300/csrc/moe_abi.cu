@@ -142,8 +142,8 @@ int check_forward_args(const moe_shape* s, const void* x, const void* w_gate, co
     return rc;
 }
 
-// The whole block.  At small S the top-k and the sort share one kernel (one
-// launch and one global round trip of the ids fewer).
+// The whole block.  At small S the top-k, the sort and the gather share one
+// kernel (two launches and two kernel boundaries fewer).
 static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     if (!topk_sort_fits(s)) {
         const int rc = run_route(s, L, p, st);
@@ -354,19 +354,19 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     if (rc) return rc;
     // A small pinned host buffer is read or written in place by the kernels
     // (measured faster than a copy): x when the router reads all of it in one
-    // round of loads (S <= 8), ids and weights when only the fused top-k +
-    // sort writes them and nothing reads them back, out up to 256 KB.  Every
-    // other buffer goes through the workspace's host-I/O staging regions
-    // (xin, hio_ids, hio_w, hio_out) and one copy, which moves bulk data
-    // faster than the kernels' own loads and stores over the link.
+    // round of loads (S <= 8), ids and weights when the fused top-k + sort +
+    // gather writes them (one CTA a pick), out up to 256 KB.  Every other
+    // buffer goes through the workspace's host-I/O staging regions (xin,
+    // hio_ids, hio_w, hio_out) and one copy, which moves bulk data faster than
+    // the kernels' own loads and stores over the link.
     WsLayout L = ws_layout(*shape);
     cudaStream_t st = (cudaStream_t)stream;
     char* w = (char*)ws;
     const size_t P = (size_t)shape->S * shape->k;
     const bool small_out = (size_t)shape->S * shape->d * 4 <= (256u << 10);
     void* x_dev = shape->S <= 8 ? device_view(x_host) : nullptr;
-    int32_t* ids_dev = ids_host && topk_sort_fits(*shape) ? (int32_t*)device_view(ids_host) : nullptr;
-    float* wts_dev = weights_host && topk_sort_fits(*shape) ? (float*)device_view(weights_host) : nullptr;
+    int32_t* ids_dev = ids_host && route_gather_selects(*shape) ? (int32_t*)device_view(ids_host) : nullptr;
+    float* wts_dev = weights_host && route_gather_selects(*shape) ? (float*)device_view(weights_host) : nullptr;
     float* out_dev = small_out ? (float*)device_view(out_host) : nullptr;
     const bool ids_staged = !ids_dev, wts_staged = !wts_dev, out_staged = !out_dev;
     if (!ids_dev) ids_dev = (int32_t*)(w + L.hio_ids);

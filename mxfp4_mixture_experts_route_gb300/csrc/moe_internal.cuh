@@ -120,11 +120,47 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // per-kernel timing hooks (moe_timing_*): no-ops unless enabled
 // ---------------------------------------------------------------------------
 enum KernelId {
-    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_TOPK_SORT,
+    K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_ROUTE_GATHER,
     K_LATENT_DOWN, K_LATENT_NORM, K_LATENT_UP, K_SHARED_GU, K_SHARED_ACT, K_SHARED_DOWN, K_NUM
 };
 void timing_begin(int kernel_id, cudaStream_t st);
 void timing_end(cudaStream_t st);
+
+// Diagnostics build (-DMOE_TRACE): every CTA of the library's kernels stamps
+// %globaltimer at its start (point 0), after its wait on the preceding kernel
+// (1), at its end (2) and at kernel-specific points 3..7 into a table
+// [K_NUM][8 points][min, max] (moe_ktrace).  The table lives in device memory the trace
+// build allocates (timing.cu); each translation unit binds its own copy of the
+// pointer before its first launch.
+#ifdef MOE_TRACE
+constexpr int KT_SLOTS = 16;
+extern unsigned long long* g_kt_dev;
+static __constant__ unsigned long long* g_ktp;
+static bool g_kt_bound = false;
+static inline void kt_bind() {
+    if (!g_kt_bound && g_kt_dev != nullptr) {
+        cudaMemcpyToSymbol(g_ktp, &g_kt_dev, sizeof(g_kt_dev));
+        g_kt_bound = true;
+    }
+}
+// what: 0 start, 1 after the wait, 2 end, 3..7 inner points (thread 0 of the CTA)
+__device__ __forceinline__ void kt_mark(int kid, int what) {
+    if (threadIdx.x != 0 || threadIdx.y != 0 || g_ktp == nullptr) return;
+    unsigned long long t;
+    asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+    atomicMin(g_ktp + kid * KT_SLOTS + 2 * what, t);
+    atomicMax(g_ktp + kid * KT_SLOTS + 2 * what + 1, t);
+}
+#define KT_BIND() kt_bind()
+#define KT_MARK(kid, what) kt_mark(kid, what)
+#else
+#define KT_BIND() \
+    do {          \
+    } while (0)
+#define KT_MARK(kid, what) \
+    do {                   \
+    } while (0)
+#endif
 
 // ---------------------------------------------------------------------------
 // launchers (one per kernel); all return cudaGetLastError() of the launch
@@ -156,9 +192,13 @@ enum DenseOut { DENSE_F32 = 0, DENSE_F32_ADD = 1, DENSE_BF16 = 2 };
 bool dense_fits(int S, int K, int N);
 cudaError_t launch_dense(const void* x, const void* w, int S, int K, int N, const float* off, void* out, int mode,
                          StatusBlock* sb, cudaStream_t st);
+cudaError_t launch_topk(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
-// moe_forward at small S: top-k and sort in one kernel (needs the logits)
+// moe_forward at small S: top-k, sort and gather in one kernel (needs the
+// logits); above 128 picks the top-k kernel first, then sort and gather
 bool topk_sort_fits(const moe_shape& s);
+// ... and the fused kernel selects the top k itself (no top-k kernel before it)
+bool route_gather_selects(const moe_shape& s);
 cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);

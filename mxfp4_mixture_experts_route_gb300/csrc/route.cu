@@ -48,6 +48,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
                                                        int S, int d, int E, int kslices) {
     __shared__ uint4 xs_[RT_TOKENS * (RT_KC / 8)];
     __shared__ float part[RT_TOKENS * RT_EXPERTS];
+    KT_MARK(K_ROUTER, 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * RT_EXPERTS + warp, ks = blockIdx.y, t0 = blockIdx.z * RT_TOKENS;
     const int nk = d / 128;                                  // 128-K units of a row
@@ -65,6 +66,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
         if (kc == k_begin) {
             pdl_wait();      // the first weight slice is in flight; x may come from the stream's last kernel
             pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
+            KT_MARK(K_ROUTER, 1);
         }
         __syncthreads();
         for (int i = threadIdx.x; i < nt * q16; i += RT_THREADS) {
@@ -116,6 +118,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
         if (t < nt && eg < E) L[(size_t)(t0 + t) * E + eg] = off ? z + off[eg] : z;
     }
     cluster.sync();   // every CTA keeps its shared memory until the first has read it
+    KT_MARK(K_ROUTER, 2);
 }
 
 // The same logits for a few tokens (S <= NTOK) and at most NR 256-K rounds per
@@ -128,6 +131,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* 
                                                            const float* __restrict__ off, float* __restrict__ L,
                                                            int S, int d, int E, int kslices) {
     __shared__ float part[NTOK * RT_EXPERTS];
+    KT_MARK(K_ROUTER, 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     const int e = blockIdx.x * RT_EXPERTS + warp, ks = blockIdx.y;
     const int nk = d / 128;
@@ -144,6 +148,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* 
     }
     pdl_wait();      // x may come from the stream's previous kernel
     pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
+    KT_MARK(K_ROUTER, 1);
     uint4 xv[NR][NTOK];
 #pragma unroll
     for (int r = 0; r < NR; ++r)
@@ -173,12 +178,14 @@ __global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* 
         for (int m = 16; m >= 1; m >>= 1) a += __shfl_xor_sync(0xffffffffu, a, m);
         acc[t] = a;
     }
+    KT_MARK(K_ROUTER, 3);
     if (lane == 0) {
 #pragma unroll
         for (int t = 0; t < NTOK; ++t) part[t * RT_EXPERTS + warp] = acc[t];
     }
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
+    KT_MARK(K_ROUTER, 4);
     if (ks == 0 && threadIdx.x < NTOK * RT_EXPERTS) {
         const int t = threadIdx.x / RT_EXPERTS, ee = threadIdx.x % RT_EXPERTS;
         const int eg = blockIdx.x * RT_EXPERTS + ee;
@@ -192,26 +199,42 @@ __global__ void __launch_bounds__(RT_THREADS) k_router_few(const __nv_bfloat16* 
         if (t < S && eg < E) L[(size_t)t * E + eg] = off ? z + off[eg] : z;
     }
     cluster.sync();
+    KT_MARK(K_ROUTER, 2);
 }
 
-// One warp per token (see topk_token).
-__global__ void __launch_bounds__(256) k_topk(const float* L, const float* __restrict__ bias,
-                                              int S, int E, int k, int32_t* __restrict__ ids,
-                                              float* __restrict__ wout) {
-    const int lane = threadIdx.x & 31;
-    pdl_trigger();
+// One warp per token (see topk_select).
+template <int MAXE>
+__device__ __forceinline__ void topk_rows(const float* L, const float* __restrict__ bias, int S, int E, int k,
+                                          int32_t* __restrict__ ids, float* __restrict__ wout, float* s_sh) {
+    const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
     const int t = (blockIdx.x * blockDim.x + threadIdx.x) >> 5;
-    if (E <= 256) {
-        float b[256 / 32];
-        load_bias(bias, E, lane, b);   // an input of the call: read before the wait
-        pdl_wait();
-        if (t < S) topk_token(L + (size_t)t * E, b, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
-    } else {
-        float b[512 / 32];
-        load_bias(bias, E, lane, b);
-        pdl_wait();
-        if (t < S) topk_token(L + (size_t)t * E, b, E, k, lane, ids + (size_t)t * k, wout + (size_t)t * k);
+    float b[MAXE];
+    load_bias(bias, E, lane, b);   // an input of the call: read before the wait
+    pdl_wait();
+    KT_MARK(K_TOPK, 1);
+    if (t < S) {
+        int id, rank;
+        float w;
+        float z[MAXE];
+        topk_load(L + (size_t)t * E, E, lane, z);
+        topk_select(z, b, E, k, lane, s_sh + warp * 32 * MAXE, id, w, rank);
+        if (lane < k) {
+            ids[(size_t)t * k + rank] = id;
+            wout[(size_t)t * k + rank] = w;
+        }
     }
+}
+
+constexpr int TOPK_WARPS = 8;
+__global__ void __launch_bounds__(32 * TOPK_WARPS) k_topk(const float* L, const float* __restrict__ bias,
+                                                          int S, int E, int k, int32_t* __restrict__ ids,
+                                                          float* __restrict__ wout) {
+    __shared__ float s_sh[TOPK_WARPS * 512];
+    KT_MARK(K_TOPK, 0);
+    pdl_trigger();
+    if (E <= 256) topk_rows<256 / 32>(L, bias, S, E, k, ids, wout, s_sh);
+    else topk_rows<512 / 32>(L, bias, S, E, k, ids, wout, s_sh);
+    KT_MARK(K_TOPK, 2);
 }
 
 }  // namespace
@@ -227,6 +250,7 @@ int router_kslices(const moe_shape& s, int num_sms) {
 }
 
 cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    KT_BIND();
     if (router_tc_fits(s)) {
         timing_begin(K_ROUTER, st);
         const cudaError_t e = launch_router_tc(s, L, p, st);
@@ -261,15 +285,20 @@ cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Pt
     return e;
 }
 
-cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    cudaError_t e = launch_router_logits(s, L, p, st);
-    if (e != cudaSuccess) return e;
-    const int warps_per_block = 8;
+cudaError_t launch_topk(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    KT_BIND();
     timing_begin(K_TOPK, st);
-    e = launch_pdl(k_topk, dim3((s.S + warps_per_block - 1) / warps_per_block), dim3(32 * warps_per_block), 0, st,
+    const cudaError_t e =
+        launch_pdl(k_topk, dim3((s.S + TOPK_WARPS - 1) / TOPK_WARPS), dim3(32 * TOPK_WARPS), 0, st,
                    reinterpret_cast<const float*>(p.ws + L.logits), p.bias, s.S, s.E, s.k, p.ids, p.weights);
     timing_end(st);
     return e;
+}
+
+cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    cudaError_t e = launch_router_logits(s, L, p, st);
+    if (e != cudaSuccess) return e;
+    return launch_topk(s, L, p, st);
 }
 
 }  // namespace moe

@@ -35,12 +35,11 @@ __host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
 
 // The pairwise-count sort (sort_picks_small) for up to SMALL_SORT_PICKS picks:
 // each thread then compares at most 16 keys for the pick it counts for; above
-// that the atomic-rank sort (sort_picks).  Shared memory of a sort kernel: the
-// chosen sort's ints, and the ids when they are staged there (always for the
-// pairwise count; for the atomic-rank sort only in the fused top-k + sort).
+// that the atomic-rank sort (sort_picks).  Shared memory of the sort kernel:
+// the chosen sort's ints (the pairwise count also stages the ids there).
 constexpr int SMALL_SORT_PICKS = 128;
-__host__ __device__ constexpr int sort_smem_ints_for(int E, int P, bool ids_in_smem) {
-    return P <= SMALL_SORT_PICKS ? 3 * P : sort_smem_ints(E) + (ids_in_smem ? P : 0);
+__host__ __device__ constexpr int sort_smem_ints_for(int E, int P) {
+    return P <= SMALL_SORT_PICKS ? 3 * P : sort_smem_ints(E);
 }
 
 // Sort of the S * k picks by expert, one CTA of SORT_THREADS threads.
@@ -53,17 +52,10 @@ __host__ __device__ constexpr int sort_smem_ints_for(int E, int P, bool ids_in_s
 //      and writes tile entries (expert e, first pick, picks in the tile)
 // The order of the picks inside a segment is the order the atomics came in:
 // each pick is an independent column of the expert GEMMs, so the results do
-// not depend on it.  ids is in global memory (an earlier kernel's output, read
-// through L2) or, with SMEM_IDS, in shared memory.
+// not depend on it.  ids is in global memory (an earlier kernel's output,
+// read through L2).
 // Output: pos[S*k], tiles[n_tiles] and n_picks / n_tiles;
 // tile_ready[] zeroed.
-template <bool SMEM_IDS>
-__device__ __forceinline__ int id_at(const int32_t* ids, size_t i) {
-    if constexpr (SMEM_IDS) return ids[i];
-    else return ld_dep(ids + i);
-}
-
-template <bool SMEM_IDS>
 __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int k, const SortOut& o,
                                            int32_t* smem) {
     int32_t* cnt = smem;               // [E + 1] counts
@@ -88,9 +80,9 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
         bool ok = false;
         if (p < P) {
             const int t = p / k, j = p - t * k;
-            e = id_at<SMEM_IDS>(ids, p);
+            e = ld_dep(ids + p);
             ok = e >= 0 && e < E;
-            for (int q = 0; q < j && ok; ++q) ok = id_at<SMEM_IDS>(ids, (size_t)t * k + q) != e;
+            for (int q = 0; q < j && ok; ++q) ok = ld_dep(ids + (size_t)t * k + q) != e;
         }
         const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
         const int leader = __ffs(grp) - 1;
@@ -153,7 +145,7 @@ __device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int
     for (int p = warp * 32 + lane; p < P; p += SORT_THREADS) {
         const int r = o.pos[p];
         if (r >= 0) {
-            const int q = off[id_at<SMEM_IDS>(ids, p)] + r;
+            const int q = off[ld_dep(ids + p)] + r;
             o.pos[p] = q;
         }
     }
@@ -268,8 +260,10 @@ __device__ __forceinline__ void sort_picks_small(const int32_t* ids, int S, int 
 __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* ids, int S, int E, int k,
                                                        SortOut o) {
     extern __shared__ int32_t smem[];
+    KT_MARK(K_SORT, 0);
     pdl_wait();
     pdl_trigger();   // after the wait: see launch_gather
+    KT_MARK(K_SORT, 1);
     const int P = S * k;
     if (P <= SMALL_SORT_PICKS) {
         int32_t* sids = smem + 2 * P;
@@ -277,32 +271,9 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* ids, int S
         __syncthreads();
         sort_picks_small(sids, S, E, k, o, smem);
     } else {
-        sort_picks<false>(ids, S, E, k, o, smem);
+        sort_picks(ids, S, E, k, o, smem);
     }
-}
-
-// moe_forward at small S: the sigmoid top-k of every token (one warp a token,
-// see topk_token) and the sort of its picks in one CTA.  The ids go to the
-// caller's buffer and, for the sort, to shared memory.
-template <int MAXE>
-__global__ void __launch_bounds__(SORT_THREADS) k_topk_sort(const float* L,
-                                                            const float* __restrict__ bias, int S, int E, int k,
-                                                            int32_t* __restrict__ ids,
-                                                            float* __restrict__ weights, SortOut o) {
-    extern __shared__ int32_t smem[];
-    pdl_trigger();
-    const int P = S * k;
-    int32_t* sids = smem + (P <= SMALL_SORT_PICKS ? 2 * P : sort_smem_ints(E));   // [S][k]
-    const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-    float b[MAXE];
-    load_bias(bias, E, lane, b);   // an input of the call: read before the wait
-    pdl_wait();
-    for (int t = warp; t < S; t += SORT_THREADS / 32)
-        topk_token(L + (size_t)t * E, b, E, k, lane, sids + (size_t)t * k, weights + (size_t)t * k);
-    __syncthreads();
-    for (int i = threadIdx.x; i < S * k; i += SORT_THREADS) ids[i] = sids[i];
-    if (P <= SMALL_SORT_PICKS) sort_picks_small(sids, S, E, k, o, smem);
-    else sort_picks<true>(sids, S, E, k, o, smem);
+    KT_MARK(K_SORT, 2);
 }
 
 // Token rows of the expert GEMMs.  grid (S * k), one pick p = t * k + j a
@@ -315,6 +286,7 @@ __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __re
                                                       const int32_t* pos, int k, int d, int I, int P,
                                                       uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
                                                       uint8_t* __restrict__ hs) {
+    KT_MARK(K_GATHER, 0);
     pdl_trigger();
     const int p = blockIdx.x, t = p / k;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
@@ -325,7 +297,9 @@ __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __re
         const int c = i * (int)blockDim.x + (int)threadIdx.x;
         if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, c, c < nc);   // block-uniform condition
     }
+    KT_MARK(K_GATHER, 3);
     pdl_wait();
+    KT_MARK(K_GATHER, 1);
     const int r = ld_dep(pos + p);
     if (r < 0) return;   // not a valid pick
     const size_t tab_rows = (size_t)P + NT_MAX;
@@ -335,6 +309,136 @@ __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __re
         if (c < nc) store_chunk(q[i], c, r, d, tab_rows, xq, xs);
     }
     pad_scale_rows(r, d, I, tab_rows, xs, hs, threadIdx.x);
+    KT_MARK(K_GATHER, 2);
+}
+
+// moe_forward at small S: the top k of every token, the sort of all S * k
+// picks and the gather in one kernel.  grid (S * k), one pick p = t * k + j a
+// CTA, as the gather.  Every CTA selects every token's top k (a warp takes
+// one or two tokens, topk_select) into shared memory, from the same logits
+// with the same code, so all CTAs hold the same ids.  Each then places only
+// its own pick, as sort_picks_small would: with cnt[e] the picks of expert e,
+// r_p = sum_{e < e_p} cnt[e] + #{q < p : e_q = e_p}; a tile opens where that
+// index inside the segment is a multiple of nt, and tiles are numbered in
+// position order: sum_{e < e_p} ceil(cnt[e] / nt) + index / nt.  It writes
+// ids[p], weights[p], pos[p], that tile entry when its pick opens one, and
+// token t's row (quantised before the wait) at r_p; CTA 0 writes the counts.
+// The picks of a token are distinct valid experts.  With FROM_IDS the ids
+// come from the top-k kernel instead (more tokens than each CTA should select
+// again): every CTA reads them and only places and gathers.
+constexpr int RG_THREADS = 512;        // at most; 16 warps: two tokens a warp at S = 32
+constexpr int RG_PASSES = 4;           // chunks of 8 elements a thread, at most: d <= 16384
+constexpr int RG_TOKENS_PER_WARP = 2;
+template <int MAXE, int PASSES, bool FROM_IDS>
+__global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, const float* __restrict__ bias,
+                                                            const __nv_bfloat16* __restrict__ x, int S, int E,
+                                                            int k, int d, int I, int P_tab,
+                                                            int32_t* __restrict__ ids, float* __restrict__ weights,
+                                                            SortOut o, uint8_t* __restrict__ xq,
+                                                            uint8_t* __restrict__ xs, uint8_t* __restrict__ hs) {
+    extern __shared__ int32_t smem[];
+    KT_MARK(K_ROUTE_GATHER, 0);
+    pdl_trigger();
+    const int P = S * k, nt = o.nt;
+    __shared__ int32_t r_sh;
+    int32_t* key = smem;           // [P] expert of pick q = t * k + j
+    int32_t* cnt = key + P;        // [E] picks of expert e
+    float* s_sh = reinterpret_cast<float*>(cnt + E);   // [min(S, warps)][32 * MAXE]
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)blockDim.x >> 5;
+    const int p = blockIdx.x, t = p / k;
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    const int nc = d / 8;
+    QuantChunk q[PASSES];
+#pragma unroll
+    for (int i = 0; i < PASSES; ++i) {
+        const int c = i * (int)blockDim.x + tid;
+        if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, c, c < nc);   // block-uniform condition
+    }
+    float b[MAXE];
+    if constexpr (!FROM_IDS) load_bias(bias, E, lane, b);
+    for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
+    pdl_wait();
+    KT_MARK(K_ROUTE_GATHER, 1);
+    if constexpr (FROM_IDS) {
+        for (int i = tid; i < P; i += blockDim.x) key[i] = ld_dep(ids + i);
+    } else {
+        // the warp's tokens warp and warp + nw: both rows of logits in flight first
+        float z[RG_TOKENS_PER_WARP][MAXE];
+#pragma unroll
+        for (int u = 0; u < RG_TOKENS_PER_WARP; ++u)
+            if (warp + u * nw < S) topk_load(L + (size_t)(warp + u * nw) * E, E, lane, z[u]);
+#pragma unroll
+        for (int u = 0; u < RG_TOKENS_PER_WARP; ++u) {
+            const int tt = warp + u * nw;
+            if (tt < S) {
+                int id, rank;
+                float w;
+                topk_select(z[u], b, E, k, lane, s_sh + warp * 32 * MAXE, id, w, rank);
+                if (lane < k) {
+                    key[tt * k + rank] = id;
+                    if (tt * k + rank == p) {
+                        ids[p] = id;
+                        weights[p] = w;
+                    }
+                }
+            }
+        }
+    }
+    __syncthreads();
+    KT_MARK(K_ROUTE_GATHER, 3);
+    for (int i = tid; i < P; i += blockDim.x) atomicAdd(&cnt[key[i]], 1);
+    __syncthreads();
+    if (warp == 0) {
+        const int ep = key[p];
+        int off = 0, toff = 0, ntiles = 0;
+        for (int e0 = 0; e0 < E; e0 += 32) {
+            const int e = e0 + lane;
+            const int n = e < E ? cnt[e] : 0;
+            const int tn = (n + nt - 1) / nt;
+            off += e < ep ? n : 0;
+            toff += e < ep ? tn : 0;
+            ntiles += tn;
+        }
+        off = __reduce_add_sync(0xffffffffu, off);
+        toff = __reduce_add_sync(0xffffffffu, toff);
+        ntiles = __reduce_add_sync(0xffffffffu, ntiles);
+        int idx = 0;   // picks of expert ep before p
+        for (int q0 = 0; q0 < p; q0 += 32) {
+            const int qq = q0 + lane;
+            idx += __popc(__ballot_sync(0xffffffffu, qq < p && key[qq] == ep));
+        }
+        if (lane == 0) {
+            const int r = off + idx;
+            r_sh = r;
+            o.pos[p] = r;
+            if (idx % nt == 0) {
+                Tile tl;
+                tl.e = ep;
+                tl.p0 = r;
+                tl.n = min(nt, cnt[ep] - idx);
+                tl.pad = 0;
+                o.tiles[toff + idx / nt] = tl;
+            }
+            if (p == 0) {
+                o.sb->n_picks = P;
+                o.sb->n_tiles = ntiles;
+                o.sb->work_next = 0;
+                o.sb->work_next2 = 0;
+            }
+        }
+    }
+    __syncthreads();
+    KT_MARK(K_ROUTE_GATHER, 4);
+    const int r = r_sh;
+    for (int i = p + (int)gridDim.x * tid; i < o.max_tiles; i += (int)gridDim.x * (int)blockDim.x) o.tile_ready[i] = 0u;
+    const size_t tab_rows = (size_t)P_tab + NT_MAX;
+#pragma unroll
+    for (int i = 0; i < PASSES; ++i) {
+        const int cc = i * (int)blockDim.x + tid;
+        if (cc < nc) store_chunk(q[i], cc, r, d, tab_rows, xq, xs);
+    }
+    pad_scale_rows(r, d, I, tab_rows, xs, hs, tid);
+    KT_MARK(K_ROUTE_GATHER, 2);
 }
 
 }  // namespace
@@ -356,6 +460,7 @@ static SortOut sort_out(const WsLayout& L, char* ws) {
 // before the call -- which wrote x -- has completed.
 static cudaError_t launch_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     char* ws = p.ws;
+    KT_BIND();
     timing_begin(K_GATHER, st);
     const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
     const cudaError_t e = launch_pdl(k_quant_gather, dim3(s.S * s.k), dim3(threads), 0, st, p.x,
@@ -367,7 +472,8 @@ static cudaError_t launch_gather(const moe_shape& s, const WsLayout& L, const Pt
 }
 
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    const size_t smem = (size_t)sort_smem_ints_for(s.E, s.S * s.k, false) * sizeof(int32_t);
+    KT_BIND();
+    const size_t smem = (size_t)sort_smem_ints_for(s.E, s.S * s.k) * sizeof(int32_t);
     timing_begin(K_SORT, st);
     cudaError_t e = launch_pdl(k_sort, dim3(1), dim3(SORT_THREADS), smem, st, (const int32_t*)p.ids, s.S, s.E, s.k,
                                sort_out(L, p.ws));
@@ -376,23 +482,57 @@ cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs
     return launch_gather(s, L, p, st);
 }
 
+// The fused top-k + sort + gather selects again in every CTA; above this
+// many picks (as many CTAs) the top-k kernel selects once and the fused
+// kernel only sorts and gathers.
+constexpr int RG_MAX_SELECT_PICKS = 128;
+
 bool topk_sort_fits(const moe_shape& s) {
-    // one token a warp (beyond that the top-k kernel spreads the tokens over
-    // more SMs), and one thread a pick for the pairwise-count sort
-    return s.S <= SORT_THREADS / 32 && s.S * s.k <= SORT_THREADS;
+    // a CTA's threads hold the row's chunks (RG_PASSES a thread), its warps
+    // one or two tokens each
+    return s.S <= RG_TOKENS_PER_WARP * (RG_THREADS / 32) && s.S * s.k <= 1024 &&
+           s.d / 8 <= RG_PASSES * RG_THREADS;
+}
+
+bool route_gather_selects(const moe_shape& s) { return topk_sort_fits(s) && s.S * s.k <= RG_MAX_SELECT_PICKS; }
+
+// a thread per chunk of 8 elements of a row, and a warp for every two tokens
+// (at least), within RG_THREADS
+static int route_gather_threads(const moe_shape& s) {
+    const int rows = (s.d / 8 + 31) / 32 * 32;
+    const int tok = 32 * ((s.S + RG_TOKENS_PER_WARP - 1) / RG_TOKENS_PER_WARP);
+    return std::min(RG_THREADS, std::max(rows, tok));
+}
+
+template <int MAXE, bool FROM_IDS>
+static cudaError_t launch_rg(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    const int threads = route_gather_threads(s);
+    const int P = s.S * s.k;
+    const size_t smem = (size_t)(P + s.E) * sizeof(int32_t) +
+                        (FROM_IDS ? 0 : (size_t)std::min(s.S, threads / 32) * 32 * MAXE * sizeof(float));
+    const int passes = (s.d / 8 + threads - 1) / threads;   // 1, 2 or 4 (d <= 16384)
+    auto kern = passes == 1 ? k_route_gather<MAXE, 1, FROM_IDS>
+                            : passes == 2 ? k_route_gather<MAXE, 2, FROM_IDS> : k_route_gather<MAXE, 4, FROM_IDS>;
+    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    char* ws = p.ws;
+    timing_begin(FROM_IDS ? K_GATHER : K_ROUTE_GATHER, st);
+    e = launch_pdl(kern, dim3(P), dim3(threads), smem, st, reinterpret_cast<const float*>(ws + L.logits), p.bias,
+                   p.x, s.S, s.E, s.k, s.d, s.I, L.max_picks, p.ids, p.weights, sort_out(L, ws),
+                   reinterpret_cast<uint8_t*>(ws + L.xq), reinterpret_cast<uint8_t*>(ws + L.xs),
+                   reinterpret_cast<uint8_t*>(ws + L.hs));
+    timing_end(st);
+    return e;
 }
 
 cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    const size_t smem = (size_t)sort_smem_ints_for(s.E, s.S * s.k, true) * sizeof(int32_t);
-    auto kern = s.E <= 256 ? k_topk_sort<256 / 32> : k_topk_sort<512 / 32>;
-    cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    timing_begin(K_TOPK_SORT, st);
-    e = launch_pdl(kern, dim3(1), dim3(SORT_THREADS), smem, st, reinterpret_cast<const float*>(p.ws + L.logits),
-                   p.bias, s.S, s.E, s.k, p.ids, p.weights, sort_out(L, p.ws));
-    timing_end(st);
-    if (e != cudaSuccess) return e;
-    return launch_gather(s, L, p, st);
+    KT_BIND();
+    if (!route_gather_selects(s)) {
+        cudaError_t e = launch_topk(s, L, p, st);
+        if (e != cudaSuccess) return e;
+        return launch_rg<8, true>(s, L, p, st);
+    }
+    return s.E <= 256 ? launch_rg<8, false>(s, L, p, st) : launch_rg<16, false>(s, L, p, st);
 }
 
 }  // namespace moe

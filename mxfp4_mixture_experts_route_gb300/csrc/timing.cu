@@ -17,7 +17,7 @@ std::vector<Rec> g_recs;   // event pairs, created by moe_timing_enable
 int g_used = 0;            // pairs recorded since the last collect
 int g_open = -1;           // pair started by timing_begin, not yet ended
 
-const char* const kNames[K_NUM] = {"router_logits", "topk", "sort", "gather", "experts", "combine", "topk_sort",
+const char* const kNames[K_NUM] = {"router_logits", "topk", "sort", "gather", "experts", "combine", "topk_sort_gather",
                                    "latent_down", "latent_norm", "latent_up", "shared_gate_up", "shared_act",
                                    "shared_down"};
 
@@ -45,6 +45,10 @@ void timing_end(cudaStream_t st) {
     cudaEventRecord(g_recs[g_open].b, st);
     g_open = -1;
 }
+
+#ifdef MOE_TRACE
+unsigned long long* g_kt_dev = nullptr;
+#endif
 
 }  // namespace moe
 
@@ -92,3 +96,22 @@ const char* moe_kernel_name(int kernel_id) {
 }
 
 }  // extern "C"
+
+#ifdef MOE_TRACE
+// Diagnostics export of the trace build: dst == NULL allocates the stamp table
+// on first use and resets it (minima to all ones, maxima to zero); otherwise
+// it synchronises the device and copies the table ([K_NUM][16] u64, see
+// kt_mark) to the host buffer dst of `bytes` bytes.
+extern "C" int moe_ktrace(unsigned long long* dst, size_t bytes) {
+    const size_t n = (size_t)K_NUM * KT_SLOTS;
+    if (g_kt_dev == nullptr && cudaMalloc(&g_kt_dev, n * sizeof(unsigned long long)) != cudaSuccess) return MOE_ERR_CUDA;
+    if (cudaDeviceSynchronize() != cudaSuccess) return MOE_ERR_CUDA;
+    if (dst == nullptr) {
+        unsigned long long init[K_NUM * KT_SLOTS];
+        for (size_t i = 0; i < n; ++i) init[i] = (i % 2 == 0) ? ~0ull : 0ull;
+        return cudaMemcpy(g_kt_dev, init, sizeof(init), cudaMemcpyHostToDevice) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+    }
+    if (bytes > n * sizeof(unsigned long long)) bytes = n * sizeof(unsigned long long);
+    return cudaMemcpy(dst, g_kt_dev, bytes, cudaMemcpyDeviceToHost) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+#endif

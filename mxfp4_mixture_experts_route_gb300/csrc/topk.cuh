@@ -1,5 +1,5 @@
 // Sigmoid top-k of one token by one warp (shared by the top-k kernel and the
-// fused top-k + sort kernel).
+// fused top-k + sort + gather kernel).
 //
 // vllm.models.muse_spark.amd.mono.kernels.k3, route_token (sigmoid scores);
 // k5, stage HA (top 8, ids and weights out).  s = sigmoid(L), sel = s + bias;
@@ -19,30 +19,6 @@ __device__ __forceinline__ uint32_t sel_key(float v) {
     return (u & 0x80000000u) ? ~u : (u | 0x80000000u);
 }
 
-// The lane's best slot: largest key, lowest slot on ties (a pairwise tree in
-// which the left operand always holds the lower slots).
-template <int MAXE>
-__device__ __forceinline__ void lane_best(const uint32_t (&key)[MAXE], uint32_t& bk, int& bi) {
-    uint32_t kk[MAXE];
-    int ii[MAXE];
-#pragma unroll
-    for (int i = 0; i < MAXE; ++i) {
-        kk[i] = key[i];
-        ii[i] = i;
-    }
-#pragma unroll
-    for (int st = 1; st < MAXE; st <<= 1) {
-#pragma unroll
-        for (int i = 0; i + st < MAXE; i += 2 * st) {
-            const bool take = kk[i + st] > kk[i];
-            kk[i] = take ? kk[i + st] : kk[i];
-            ii[i] = take ? ii[i + st] : ii[i];
-        }
-    }
-    bk = kk[0];
-    bi = ii[0];
-}
-
 // The lane's slots of the bias (lane l holds experts l, l + 32, ...).
 template <int MAXE>
 __device__ __forceinline__ void load_bias(const float* __restrict__ bias, int E, int lane, float (&b)[MAXE]) {
@@ -53,66 +29,85 @@ __device__ __forceinline__ void load_bias(const float* __restrict__ bias, int E,
     }
 }
 
-// Lane l holds experts l, l + 32, ... (E <= 32 * MAXE), b from load_bias.
-// Each round takes the warp's largest key (one redux), the lowest expert id
-// among the lanes that hold it (a second redux), and lets the owning lane
-// retire it and find its next best.  Writes ids_out[0..k) in ascending id and
-// w_out[0..k).
+// A token's logits (the router's output, read through L2): lane l gets
+// experts l, l + 32, ... (independent loads, all in flight together).
 template <int MAXE>
-__device__ __forceinline__ void topk_token(const float* Lrow, const float (&b)[MAXE], int E, int k,
-                                           int lane, int32_t* ids_out, float* w_out) {
-    float s[MAXE], z[MAXE];
-    uint32_t key[MAXE];
-#pragma unroll
-    for (int i = 0; i < MAXE; ++i) {           // independent loads, all in flight together
-        const int e = lane + 32 * i;
-        z[i] = e < E ? ld_dep(Lrow + e) : 0.f;   // the router's output
-    }
+__device__ __forceinline__ void topk_load(const float* Lrow, int E, int lane, float (&z)[MAXE]) {
 #pragma unroll
     for (int i = 0; i < MAXE; ++i) {
         const int e = lane + 32 * i;
-        s[i] = __fdividef(1.0f, 1.0f + __expf(-z[i]));   // a few ulp; the sets need score gaps far larger
-        key[i] = e < E ? sel_key(s[i] + b[i]) : 0u;
+        z[i] = e < E ? ld_dep(Lrow + e) : 0.f;
     }
-    uint32_t bk;
-    int bi;
-    lane_best(key, bk, bi);
-    int my_id = 0x7fffffff;   // lane j < k keeps pick j
-    float my_s = 0.f;
-    for (int r = 0; r < k; ++r) {
-        const uint32_t m = __reduce_max_sync(0xffffffffu, bk);
-        const uint32_t win = __reduce_min_sync(0xffffffffu, bk == m ? (uint32_t)(lane + 32 * bi) : 0xffffffffu);
-        const int owner = (int)(win & 31u);
-        float sv = 0.f;
-        if (lane == owner) {
-            const int slot = (int)(win >> 5);
+}
+
+// The top k of one token from its logits z (topk_load) and the bias b
+// (load_bias), by one warp; s_sh is the warp's scratch of 32 * MAXE floats in
+// shared memory.
+//   1. each expert's entry v = key << 32 | ~id orders by score, then by lower
+//      id; every lane sorts its MAXE entries (a bitonic network in registers,
+//      independent of the other lanes)
+//   2. k rounds: the largest key among the lanes' heads (one redux), the
+//      lowest id among the heads that hold it (a second redux; a lane's other
+//      entries of that key have higher ids than its head); the owning lane
+//      drops its head, lane r keeps round r's winner
+//   3. lane j < k: the rank of its id among the k (ascending id order), its s
+//      from s_sh and the sum of the picks' s (a butterfly over the lanes, the
+//      same in all)
+// On return lane j < k holds one pick: its id, its weight and its rank in
+// ascending id order (the caller writes it to slot rank).
+template <int MAXE>
+__device__ __forceinline__ void topk_select(const float (&z)[MAXE], const float (&b)[MAXE], int E, int k, int lane,
+                                            float* s_sh, int& id_out, float& w_out, int& rank_out) {
+    uint64_t v[MAXE];
+#pragma unroll
+    for (int i = 0; i < MAXE; ++i) {
+        const int e = lane + 32 * i;
+        const float s = __fdividef(1.0f, 1.0f + __expf(-z[i]));   // a few ulp; the sets need score gaps far larger
+        s_sh[e] = s;
+        const uint32_t key = e < E ? sel_key(s + b[i]) : 0u;
+        v[i] = (uint64_t)key << 32 | (uint64_t)(~(uint32_t)e);
+    }
+    // 1: descending
+#pragma unroll
+    for (int kk = 2; kk <= MAXE; kk <<= 1) {
+#pragma unroll
+        for (int j = kk >> 1; j > 0; j >>= 1) {
 #pragma unroll
             for (int i = 0; i < MAXE; ++i) {
-                if (i == slot) {
-                    sv = s[i];
-                    key[i] = 0u;
+                const int l = i ^ j;
+                if (l > i) {
+                    const uint64_t x0 = v[i], x1 = v[l];
+                    const bool sw = (i & kk) == 0 ? x1 > x0 : x0 > x1;
+                    v[i] = sw ? x1 : x0;
+                    v[l] = sw ? x0 : x1;
                 }
             }
-            lane_best(key, bk, bi);
-        }
-        sv = __shfl_sync(0xffffffffu, sv, owner);
-        if (lane == r) {
-            my_id = (int)win;
-            my_s = sv;
         }
     }
-    // ascending id order: rank of my pick among the k picks
-    float tot = 0.f;
+    // 2
+    int my_id = 0x7fffffff;
+    for (int r = 0; r < k; ++r) {
+        const uint32_t hk = (uint32_t)(v[0] >> 32);
+        const uint32_t m = __reduce_max_sync(0xffffffffu, hk);
+        const uint32_t win = __reduce_min_sync(0xffffffffu, hk == m ? ~(uint32_t)v[0] : 0xffffffffu);
+        const bool own = (int)(win & 31u) == lane;
+#pragma unroll
+        for (int i = 0; i + 1 < MAXE; ++i) v[i] = own ? v[i + 1] : v[i];
+        v[MAXE - 1] = own ? 0ull : v[MAXE - 1];
+        my_id = lane == r ? (int)win : my_id;
+    }
+    // 3
+    __syncwarp();
     int rank = 0;
-    for (int j = 0; j < k; ++j) {
-        const int oid = __shfl_sync(0xffffffffu, my_id, j);
-        tot += __shfl_sync(0xffffffffu, my_s, j);
-        rank += (oid < my_id) ? 1 : 0;
-    }
-    if (lane < k) {
-        ids_out[rank] = my_id;
-        w_out[rank] = my_s / tot;
-    }
+    for (int j = 0; j < k; ++j) rank += __shfl_sync(0xffffffffu, my_id, j) < my_id ? 1 : 0;
+    const float sv = lane < k ? s_sh[my_id] : 0.f;
+    float tot = sv;
+#pragma unroll
+    for (int o = 16; o >= 1; o >>= 1) tot += __shfl_xor_sync(0xffffffffu, tot, o);
+    id_out = my_id;
+    w_out = sv / tot;
+    rank_out = rank;
+    __syncwarp();   // s_sh is written again by the warp's next token
 }
 
 }  // namespace moe

@@ -236,6 +236,25 @@ def test_one_expert_takes_every_token():
     _check(inp, ids, w, out, L)
 
 
+@pytest.mark.parametrize("S", [8, 24, 40], ids=["fused_select", "topk_then_fused_sort", "topk_kernel"])
+def test_exact_ties_go_to_the_lower_id(S):
+    """Zero router weights: every logit is 0 and every score 0.5, so the
+    selection scores are the bias, drawn from three values: whole groups of
+    experts tie exactly, and the k picks must be the experts of the largest
+    bias values, lower ids first (the pages' order on equal scores: the
+    lower expert index)."""
+    cfg = mi.MoEConfig("ties", S=S, d=256, E=64, k=8, I=128)
+    inp = mi.make_inputs(cfg, 3, use_stored_attempts=False)
+    inp.w_gate = np.zeros_like(inp.w_gate)
+    rng = np.random.default_rng(5)
+    inp.bias = rng.choice(np.array([0.0, 0.25, 0.5], np.float32), size=cfg.E).astype(np.float32)
+    ids, w, out, L = gpu_forward(inp)
+    want = sorted(sorted(range(cfg.E), key=lambda e: (-float(inp.bias[e]), e))[:cfg.k])
+    assert np.array_equal(ids, np.tile(np.array(want, np.int32), (S, 1)))
+    assert np.allclose(w, 1.0 / cfg.k, rtol=1e-6, atol=0)
+    _check(inp, ids, w, out, L)
+
+
 def test_bad_ids_latch_status():
     import torch
     inp = mi.make_inputs(mi.CONFIGS[0])
