@@ -251,6 +251,26 @@ __device__ __forceinline__ int weight_row(const Unit& U, int blk, int r, int rd,
     return U.e * a.d + (U.mb * rd + blk) * AROWS + r;
 }
 
+// The CTA's first unit, unit blockIdx.x, when it is a gate_up unit (there
+// are n_tiles * I / 64 of them): the two producers compute it themselves
+// from the tile table, so that their first copies wait for no ring round
+// trip.  The scheduler publishes the same unit (from the same entries) first.
+__device__ __forceinline__ bool first_gate_up_unit(const Args& a, Unit& U) {
+    const int mb1 = a.I / 64, u = (int)blockIdx.x;
+    const int n_tiles = ld_dep(&a.sb->n_tiles);
+    const Tile tl = load_tile(a.tiles + min(u / mb1, a.max_tiles - 1));
+    if (u >= n_tiles * mb1) return false;
+    U.down = 0;
+    U.tile = u / mb1;
+    U.mb = u % mb1;
+    U.e = tl.e;
+    U.p0 = tl.p0;
+    U.n = tl.n;
+    U.nblk = 0;
+    U.stages = (a.d + KS - 1) / KS;
+    return true;
+}
+
 template <bool STMA, int NTT>
 __global__ void __launch_bounds__(NUM_THREADS, 1)
     k_experts_mx(const __grid_constant__ CUtensorMap tm_w13, const __grid_constant__ CUtensorMap tm_w2,
@@ -331,27 +351,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::prefetch_tensormap(&tm_xq);
         ptx::prefetch_tensormap(&tm_hq);
     }
+    ptx::tc_fence_before();
+    __syncthreads();
+    ptx::tc_fence_after();
+    const uint32_t tmem = *tmem_holder;
     // the set-up above needs nothing from the preceding kernels; everything
     // below reads their results
     pdl_wait();
     if (threadIdx.x == 0) MOE_TR(TR_MISC, 1);
     KT_MARK(K_EXPERTS, 1);
-    // CTA b's first unit is unit b; the later ones are claimed from the counter
-    // (offset by the grid size).  The tile count, the first unit's tile entry
-    // (read as if it were a gate_up unit, the usual case, and read again below
-    // if not) and the second claim are all in flight at once.
-    int claim1 = 0, n_tiles = 0;
-    Tile tile0 = {0, 0, 0, 0};
-    if (warp == SCHED_WARP) {
-        n_tiles = ld_dep(&sb->n_tiles);
-        tile0 = load_tile(a.tiles + min((int)blockIdx.x / (a.I / 64), a.max_tiles - 1));
-        if (lane == 0) claim1 = atomicAdd(&sb->work_next, 1);   // raw counter value
-    }
-    ptx::tc_fence_before();
-    __syncthreads();
-    ptx::tc_fence_after();
-    KT_MARK(K_EXPERTS, 3);
-    const uint32_t tmem = *tmem_holder;
 
     const int mb1 = a.I / 64;
     const int kst_down = (a.I + KS - 1) / KS;             // 256-K stages of one down row block
@@ -376,12 +384,44 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const uint64_t pol_w = ptx::policy_evict_first();
         int ts = 0;   // stage sequence number
         bool ok = true;
+        if (lane == 0) MOE_TR(TR_MISC, 7);
+        // lane 0: the weight tile (and its e8m0 bytes, STMA) of stage c of
+        // unit U into ring slot s
+        auto issue = [&](const Unit& U, const StageWalk& sa, int s) {
+            uint8_t* st = wst + s * C::A_STAGE;
+            const int r0 = U.down ? U.e * a.d + (U.mb * RD + sa.blk) * AROWS : U.mb * 64;
+            ptx::mbar_arrive_expect_tx(&full_a[s], A_TX + (STMA ? C::SC_BYTES : 0));
+            if (!U.down) {
+                // gate rows mb*64.. and up rows I + mb*64.. of expert e, 2 slabs of 128 K
+                ptx::tma_load_4d(st, &tm_w13, 0, r0, 2 * U.e, 2 * sa.kc, &full_a[s], pol_w);
+                if (STMA) ptx::tma_load_3d(st + C::SC_OFF, &tm_w13s, (sa.kc >> 1) * 16, r0, 2 * U.e, &full_a[s], pol_w);
+            } else {
+                ptx::tma_load_3d(st, &tm_w2, 0, r0, 2 * sa.kc, &full_a[s], pol_w);
+                if (STMA) ptx::tma_load_2d(st + C::SC_OFF, &tm_w2s, (sa.kc >> 1) * 16, r0, &full_a[s], pol_w);
+            }
+        };
+        // the first unit's first stages, before it comes through the ring (the
+        // ring of weight stages is empty: no slot to wait for)
+        int pre = 0;
+        if (STMA) {
+            Unit U0;
+            if (lane == 0 && first_gate_up_unit(a, U0)) {
+                pre = min(NSA, U0.stages);
+                StageWalk sa(U0, kst_down);
+                for (int c = 0; c < pre; ++c, sa.next()) {
+                    MOE_TR(TR_ISSUE, c);
+                    issue(U0, sa, c);
+                }
+            }
+            pre = __shfl_sync(0xffffffffu, pre, 0);
+        }
         for (int i = 0; ok; ++i) {
             Unit U;
             if (!take_unit(i, U)) {
                 if (lane == 0) fail(14);
                 break;
             }
+            if (lane == 0 && i == 0) MOE_TR(TR_MISC, 5);
             if (lane == 0) *taken = i + 1;
             if (lane == 0) MOE_TR(TR_UNIT, i);
 #ifdef MOE_TRACE
@@ -393,7 +433,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             const int K = U.down ? a.I : a.d;
             StageWalk sa(U, kst_down);
             for (int c = 0; c < U.stages; ++c, ++ts, sa.next()) {
-                const int r0 = U.down ? U.e * a.d + (U.mb * RD + sa.blk) * AROWS : U.mb * 64;
+                if (i == 0 && c < pre) continue;   // issued above
                 const int s = ts % NSA;
                 if (!ptx::mbar_wait_warp(&empty_a[s], ((ts / NSA) & 1) ^ 1, abort_flag, WAIT_NS)) {
                     if (lane == 0) fail(1);
@@ -403,15 +443,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 uint8_t* st = wst + s * C::A_STAGE;
                 if (lane == 0) {
                     MOE_TR(TR_ISSUE, ts);
-                    ptx::mbar_arrive_expect_tx(&full_a[s], A_TX + (STMA ? C::SC_BYTES : 0));
-                    if (!U.down) {
-                        // gate rows mb*64.. and up rows I + mb*64.. of expert e, 2 slabs of 128 K
-                        ptx::tma_load_4d(st, &tm_w13, 0, r0, 2 * U.e, 2 * sa.kc, &full_a[s], pol_w);
-                        if (STMA) ptx::tma_load_3d(st + C::SC_OFF, &tm_w13s, (sa.kc >> 1) * 16, r0, 2 * U.e, &full_a[s], pol_w);
-                    } else {
-                        ptx::tma_load_3d(st, &tm_w2, 0, r0, 2 * sa.kc, &full_a[s], pol_w);
-                        if (STMA) ptx::tma_load_2d(st + C::SC_OFF, &tm_w2s, (sa.kc >> 1) * 16, r0, &full_a[s], pol_w);
-                    }
+                    issue(U, sa, s);
                 }
                 if (!STMA) {
                     // e8m0 bytes of this stage: rows lane, lane+32, lane+64, lane+96, 4 bytes a
@@ -437,6 +469,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         ptx::cp_async_wait_all();
     } else if (warp == SCHED_WARP) {
         // ------------------------------------------------------------ unit scheduler
+        // CTA b's first unit is unit b; the later ones are claimed from the
+        // counter (offset by the grid size).  The tile count, the first unit's
+        // tile entry (read as if it were a gate_up unit, the usual case, and
+        // read again below if not) and the second claim are all in flight at
+        // once.
+        const int n_tiles = ld_dep(&sb->n_tiles);
+        const Tile tile0 = load_tile(a.tiles + min((int)blockIdx.x / mb1, a.max_tiles - 1));
+        int claim1 = 0;
+        if (lane == 0) claim1 = atomicAdd(&sb->work_next, 1);   // raw counter value
         const int U1 = n_tiles * mb1;
         const int total = U1 + n_tiles * g2;
         auto tile_of = [&](int u) { return u < U1 ? u / mb1 : (u - U1) / g2; };
@@ -449,6 +490,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         int next_claim = claim1;   // lane 0
         Tile tl = tile0, tl_next = {0, 0, 0, 0};
         int u_next = total;
+        if (lane == 0) MOE_TR(TR_MISC, 3);
         if (u >= U1 && u < total) tl = load_tile(a.tiles + tile_of(u));
         auto claim_next = [&]() {
             u_next = u < total ? (int)gridDim.x + __shfl_sync(0xffffffffu, next_claim, 0) : total;
@@ -492,6 +534,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             if (lane == 0) {
                 uring[i % UR] = U;
                 ptx::mbar_arrive(&u_full[i % UR]);
+                if (i == 0) MOE_TR(TR_MISC, 4);
             }
             if (U.down < 0) break;
             if (i == 0) claim_next();
@@ -504,6 +547,27 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const size_t tab_rows = (size_t)a.P + NT_MAX;
         int ts = 0;
         bool ok = true;
+        // lane 0: token stage kc of unit U (x rows, or h rows for a down unit)
+        // and its block scales into ring slot s
+        auto issue = [&](const Unit& U, int kc, int s) {
+            uint8_t* st = tst + s * C::B_STAGE;
+            const CUtensorMap* tmB = U.down ? &tm_hq : &tm_xq;
+            const uint8_t* tab = U.down ? a.hs : a.xs;
+            ptx::mbar_arrive_expect_tx(&full_b[s], B_SMEM + BS_BYTES);
+            ptx::tma_load_3d(st, tmB, 0, 2 * U.p0, 2 * kc, &full_b[s], pol_x);
+            ptx::bulk_load(tsc + s * BS_BYTES, tab + ((size_t)kc * tab_rows + U.p0) * TOKEN_SCALE_ROW, BS_BYTES,
+                           &full_b[s], pol_x);
+        };
+        // the first unit's first stages, before it comes through the ring
+        int pre = 0;
+        {
+            Unit U0;
+            if (lane == 0 && first_gate_up_unit(a, U0)) {
+                pre = min(NSB, U0.stages);
+                for (int c = 0; c < pre; ++c) issue(U0, c, c);   // gate_up: stage c reads K chunk c
+            }
+            pre = __shfl_sync(0xffffffffu, pre, 0);
+        }
         for (int i = 0; ok; ++i) {
             Unit U;
             if (!take_unit(i, U)) {
@@ -511,8 +575,6 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 break;
             }
             if (U.down < 0) break;
-            const CUtensorMap* tmB = U.down ? &tm_hq : &tm_xq;
-            const uint8_t* tab = U.down ? a.hs : a.xs;
             if (U.down) {
                 // the tile's h rows: complete once all its gate_up units are done
                 uint32_t ready = 0;
@@ -539,21 +601,15 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             StageWalk sw(U, kst_down);
             for (int c = 0; c < U.stages; ++c, ++ts, sw.next()) {
+                if (i == 0 && c < pre) continue;   // issued above
                 const int s = ts % NSB;
                 if (!ptx::mbar_wait_warp(&empty_b[s], ((ts / NSB) & 1) ^ 1, abort_flag, WAIT_NS)) {
                     if (lane == 0) fail(13);
                     ok = false;
                     break;
                 }
-                if (lane == 0) {
-                    // a down unit's blocks read the same h rows: stage kc of h
-                    const int kc = sw.kc;
-                    uint8_t* st = tst + s * C::B_STAGE;
-                    ptx::mbar_arrive_expect_tx(&full_b[s], B_SMEM + BS_BYTES);
-                    ptx::tma_load_3d(st, tmB, 0, 2 * U.p0, 2 * kc, &full_b[s], pol_x);
-                    ptx::bulk_load(tsc + s * BS_BYTES, tab + ((size_t)kc * tab_rows + U.p0) * TOKEN_SCALE_ROW,
-                                   BS_BYTES, &full_b[s], pol_x);
-                }
+                // a down unit's blocks read the same h rows: stage kc of h
+                if (lane == 0) issue(U, sw.kc, s);
                 __syncwarp();
             }
         }
