@@ -82,6 +82,7 @@ constexpr int A_TX = AROWS * KS / 2;         // packed bytes of a weight tile: t
 #ifndef MOE_MX_DOWN_BLOCKS
 #define MOE_MX_DOWN_BLOCKS 2
 #endif
+
 constexpr int NSB_DEF = MOE_MX_TOKEN_STAGES; // token-tile stages (MOE_MX_WIDE_TOKEN_STAGES for 64-pick tiles)
 constexpr int TMEM_COLS = 512;
 constexpr int NMMA_MAX = 2;                  // MMA-issuing warps (one thread each; one for 64-pick tiles)
@@ -94,7 +95,7 @@ constexpr int SF_SLOT = 64;
 constexpr int SF_A1 = 16, SF_B0 = 32, SF_B1 = 48;
 constexpr int MMA_WARP0 = 1, EPI_WARP0 = 3, TOK_WARP = 7, SF_WARP0 = 8, SCHED_WARP = 12;
 constexpr int NUM_WARPS = 13;
-constexpr int LOOKAHEAD = 2;                 // units the scheduler publishes ahead of the weight producer
+constexpr int LOOKAHEAD = 1;                 // units the scheduler publishes ahead of the weight producer
 constexpr int NUM_THREADS = 32 * NUM_WARPS;
 constexpr int UR = 32;                       // unit ring entries
 // Diagnostics build (-DMOE_TRACE): %globaltimer stamps per CTA, read back
@@ -123,6 +124,15 @@ constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
 constexpr uint64_t WAIT_NS = 1000000ull;
 int g_unreachable_wait = 0;
 #endif
+
+struct Unit {
+    int down;        // 0: gate_up, 1: down, -1: no more units
+    int tile, mb;    // tile index; row block (gate_up) or group of RD row blocks (down)
+    int e, p0, n;
+    int stages;      // 256-K stages of the unit
+    int nblk;        // down: 128-row blocks of the unit (<= RD)
+    int h_ready;     // down: the scheduler saw the tile's h rows complete
+};
 
 // STMA: the e8m0 bytes of the weights come by TMA, 16 bytes (512 K) of each
 // row per stage, when the scale rows are 16-byte aligned (K % 512 == 0);
@@ -161,7 +171,7 @@ struct Cfg {
     static constexpr int B_STAGE = B_SMEM;                     // the token scale rows sit apart
     static constexpr int XCH_STRIDE = EC + 1;
     static constexpr int XCH_BYTES = 64 * XCH_STRIDE * 4;
-    static constexpr int RING_BYTES = UR * 32;
+    static constexpr int RING_BYTES = (UR * (int)sizeof(Unit) + 15) / 16 * 16;
     static constexpr int TSC_BYTES = NSB * BS_BYTES;
     static constexpr int MISC = 1024 /*align slack*/ + XCH_BYTES + RING_BYTES + TSC_BYTES + 1024 /*barriers*/;
     static constexpr int NSA_FIT = (232448 - MISC - NSB * B_STAGE) / A_STAGE;
@@ -202,13 +212,6 @@ __device__ __forceinline__ Tile load_tile(const Tile* p) {
     return t;
 }
 
-struct Unit {
-    int down;        // 0: gate_up, 1: down, -1: no more units
-    int tile, mb;    // tile index; row block (gate_up) or group of RD row blocks (down)
-    int e, p0, n;
-    int stages;      // 256-K stages of the unit
-    int nblk;        // down: 128-row blocks of the unit (<= RD)
-};
 
 // unit u of the call (u < U1: gate_up units, tile-major; then down units, g2
 // groups of rd row blocks a tile)
@@ -268,6 +271,7 @@ __device__ __forceinline__ bool first_gate_up_unit(const Args& a, Unit& U) {
     U.n = tl.n;
     U.nblk = 0;
     U.stages = (a.d + KS - 1) / KS;
+    U.h_ready = 0;
     return true;
 }
 
@@ -365,6 +369,16 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
     const int kst_down = (a.I + KS - 1) / KS;             // 256-K stages of one down row block
     const int mb2 = a.d / AROWS;                          // 128-row blocks of w2 per expert
     const int g2 = (mb2 + RD - 1) / RD;                   // down units per tile
+    // a down unit's h rows are complete when all mb1 gate_up units of its
+    // tile have counted themselves in tile_ready
+    auto h_target = [&](const Unit& U) -> uint32_t {
+#ifndef MOE_WAIT_TEST
+        return (uint32_t)mb1;
+#else
+        return (uint32_t)mb1 + (a.unreachable && U.tile == 0 && U.mb == 0 ? 1u : 0u);
+#endif
+    };
+    auto ld_acquire_h = [&](const Unit& U) -> uint32_t { return ptx::ld_acquire_gpu(&a.tile_ready[U.tile]); };
 
     auto fail = [&](int site) {
         latch_status(sb, MOE_ERR_TIMEOUT, site);
@@ -481,22 +495,18 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
         const int U1 = n_tiles * mb1;
         const int total = U1 + n_tiles * g2;
         auto tile_of = [&](int u) { return u < U1 ? u / mb1 : (u - U1) / g2; };
-        // Unit u and its tile entry; the claim of the next unit and its tile
-        // entry are in flight while this one waits for its turn (a claim is
-        // kept as the raw counter value until it is used: arithmetic on it
-        // would wait for the atomic).  The CTA's first unit is published
-        // before that, so that its weights stream without waiting for a claim.
+        // Ring entry i is published once the weight producer has taken entry
+        // i - 1, and only then is entry i + 1 claimed (its claim, then its tile
+        // entry: a round trip of about two unit-stages, hidden behind the
+        // stages of entry i - 1 and i still to issue).  So a CTA holds at most
+        // two units beyond the one it streams when the counter runs out, and
+        // the CTAs end within about a unit of one another.  Entry 1's claim
+        // was issued at the start (a claim is kept as the raw counter value
+        // until it is used: arithmetic on it would wait for the atomic).
         int u = (int)blockIdx.x;
-        int next_claim = claim1;   // lane 0
-        Tile tl = tile0, tl_next = {0, 0, 0, 0};
-        int u_next = total;
+        Tile tl = tile0;
         if (lane == 0) MOE_TR(TR_MISC, 3);
         if (u >= U1 && u < total) tl = load_tile(a.tiles + tile_of(u));
-        auto claim_next = [&]() {
-            u_next = u < total ? (int)gridDim.x + __shfl_sync(0xffffffffu, next_claim, 0) : total;
-            if (u_next < total) tl_next = load_tile(a.tiles + tile_of(u_next));
-            if (lane == 0) next_claim = u_next < total ? atomicAdd(&sb->work_next, 1) : total;
-        };
         for (int i = 0;; ++i) {
             Unit U;
             if (u < total) {
@@ -506,13 +516,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 U.n = tl.n;
                 U.nblk = U.down ? min(RD, mb2 - U.mb * RD) : 0;
                 U.stages = U.down ? U.nblk * kst_down : (a.d + KS - 1) / KS;
+                // a down unit's h rows, read now (a unit before the token
+                // producer needs them): when complete, it skips its own wait
+                U.h_ready = U.down ? (int)(ld_acquire_h(U) >= h_target(U)) : 0;
             } else {
                 U.down = -1;
-                U.tile = U.mb = U.e = U.p0 = U.n = U.stages = U.nblk = 0;
+                U.tile = U.mb = U.e = U.p0 = U.n = U.stages = U.nblk = U.h_ready = 0;
             }
-            if (i > 0) claim_next();
-            // publish unit i once the weight producer has taken unit i - LOOKAHEAD
-            // (bounded): claimed units wait in this CTA for a short while only
             bool go = true;
             if (lane == 0 && i >= LOOKAHEAD) {
                 const uint64_t t0 = ptx::globaltimer();
@@ -537,9 +547,11 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 if (i == 0) MOE_TR(TR_MISC, 4);
             }
             if (U.down < 0) break;
-            if (i == 0) claim_next();
-            u = u_next;
-            tl = tl_next;
+            int claim = claim1;
+            if (i > 0 && lane == 0) claim = atomicAdd(&sb->work_next, 1);
+            u = (int)gridDim.x + __shfl_sync(0xffffffffu, claim, 0);
+            if (u < total) tl = load_tile(a.tiles + tile_of(u));
+            else u = total;
         }
     } else if (warp == TOK_WARP) {
         // ------------------------------------------------------------ token producer
@@ -576,18 +588,17 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
             }
             if (U.down < 0) break;
             if (U.down) {
-                // the tile's h rows: complete once all its gate_up units are done
+                // the tile's h rows: complete once all its gate_up units are
+                // done (seen by the scheduler already, or waited for here);
+                // the scheduler's acquire orders them before its ring entry,
+                // which this warp's wait on the entry orders before its copies
                 uint32_t ready = 0;
                 if (lane == 0) {
                     const uint64_t t0 = ptx::globaltimer();
                     uint32_t it = 0;
                     ready = 1;
-#ifndef MOE_WAIT_TEST
-                    const uint32_t target = (uint32_t)mb1;
-#else
-                    const uint32_t target = (uint32_t)mb1 + (a.unreachable && U.tile == 0 && U.mb == 0 ? 1u : 0u);
-#endif
-                    while (ptx::ld_acquire_gpu(&a.tile_ready[U.tile]) < target) {
+                    const uint32_t target = h_target(U);
+                    while (!U.h_ready && ptx::ld_acquire_gpu(&a.tile_ready[U.tile]) < target) {
                         __nanosleep(32);
                         if ((++it & 63u) == 0u && (*abort_flag || ptx::globaltimer() - t0 > WAIT_NS)) {
                             fail(2);
