@@ -301,6 +301,7 @@ int latent_layout(const moe_latent_shape* ls, LatentLayout& o) {
     if (ls->flags & ~MOE_LOGIT_OFFSET) return MOE_ERR_INVALID_ARG;
     if (ls->SI < 0 || ls->H < 1 || ls->LAT < 1) return MOE_ERR_INVALID_ARG;
     if (ls->SI % 128 || ls->SI > 16384) return MOE_ERR_UNSUPPORTED_SHAPE;
+    if (!latent_mid_fits(ls->LAT)) return MOE_ERR_UNSUPPORTED_SHAPE;
     o.sr = moe_shape{ls->S, ls->H, ls->E, ls->k, ls->I, ls->flags, ls->norm_eps};
     o.sx = moe_shape{ls->S, ls->LAT, ls->E, ls->k, ls->I, 0u, ls->norm_eps};
     int rc = check_shape(&o.sr);
@@ -426,7 +427,16 @@ int moe_latent_forward(const moe_latent_shape* shape, const void* x, const void*
     char* w = (char*)ws;
     StatusBlock* sb = reinterpret_cast<StatusBlock*>(w + LL.Lr.status);
     const int S = ls.S;
-    // route over the layer input (k2 page: the router parts read x)
+    // k2 page, K2b's stages, in seven launches at small S:
+    //   1. the router's logits over the layer input x (over H)
+    //   2. latent down xl = bf16(x . w_ld^T) and the shared expert's gate/up
+    //      gu = x . w_sgu^T, one launch (the same x, the weights one after the other)
+    //   3. top-k, sort and gather of xl (the block's workspace over LAT shares
+    //      the router's status, logits, pos and tile regions)
+    //   4-5. the expert GEMMs and the combine: yl
+    //   6. zl = bf16(RMSNorm(yl) ln_w) and hs = bf16(silu(g) u)
+    //   7. out = zl . w_up^T + hs . w_sd^T, one launch (the two products
+    //      concatenated along K)
     Ptrs pr{};
     pr.x = (const __nv_bfloat16*)x;
     pr.w_gate = (const __nv_bfloat16*)w_gate;
@@ -435,44 +445,48 @@ int moe_latent_forward(const moe_latent_shape* shape, const void* x, const void*
     pr.ids = ids;
     pr.weights = weights;
     pr.ws = w;
-    rc = run_route(LL.sr, LL.Lr, pr, st);
-    // latent parts: xl = x . w_ld^T (bf16)
-    auto dense = [&](int kid, const void* in, const void* wt, int K, int N, void* o, int mode) {
-        if (rc) return;
-        timing_begin(kid, st);
-        rc = cuda_rc(launch_dense(in, wt, S, K, N, nullptr, o, mode, sb, st));
-        timing_end(st);
-    };
-    dense(K_LATENT_DOWN, x, w_ld, ls.H, ls.LAT, w + LL.xl, DENSE_BF16);
-    // the routed block on the latent rows
+    rc = cuda_rc(launch_router_logits(LL.sr, LL.Lr, pr, st));
     if (!rc) {
-        Ptrs px{};
-        px.x = (const __nv_bfloat16*)(w + LL.xl);
-        px.ids = ids;
-        px.weights = weights;
-        px.w13 = w13; px.w13s = w13s; px.w2 = w2; px.w2s = w2s;
-        px.norm_w = nullptr;
-        px.out = (float*)(w + LL.yl);
-        px.ws = w;
-        rc = run_experts(LL.sx, LL.Lx, px, st);
-    }
-    // lnorm, up
-    if (!rc) {
-        timing_begin(K_LATENT_NORM, st);
-        rc = cuda_rc(launch_latent_norm((const float*)(w + LL.yl), ln_w, ls.norm_eps, S, ls.LAT,
-                                        (__nv_bfloat16*)(w + LL.zl), st));
+        timing_begin(K_LATENT_DOWN, st);
+        rc = shared ? cuda_rc(launch_dense_ncat(x, S, ls.H, w_ld, ls.LAT, w + LL.xl, DENSE_BF16, w_sgu, 2 * ls.SI,
+                                                w + LL.gu, DENSE_F32, sb, st, K_LATENT_DOWN))
+                    : cuda_rc(launch_dense(x, w_ld, S, ls.H, ls.LAT, nullptr, w + LL.xl, DENSE_BF16, sb, st,
+                                           K_LATENT_DOWN));
         timing_end(st);
     }
-    dense(K_LATENT_UP, w + LL.zl, w_up, ls.LAT, ls.H, out, DENSE_F32);
-    // the shared expert on the layer input, added to the output
-    if (shared) {
-        dense(K_SHARED_GU, x, w_sgu, ls.H, 2 * ls.SI, w + LL.gu, DENSE_F32);
-        if (!rc) {
-            timing_begin(K_SHARED_ACT, st);
-            rc = cuda_rc(launch_shared_act((const float*)(w + LL.gu), S, ls.SI, (__nv_bfloat16*)(w + LL.hs), st));
-            timing_end(st);
+    Ptrs px{};
+    px.x = (const __nv_bfloat16*)(w + LL.xl);
+    px.bias = bias;
+    px.ids = ids;
+    px.weights = weights;
+    px.w13 = w13; px.w13s = w13s; px.w2 = w2; px.w2s = w2s;
+    px.norm_w = nullptr;
+    px.out = (float*)(w + LL.yl);
+    px.ws = w;
+    if (!rc) {
+        if (topk_sort_fits(LL.sx)) {
+            rc = cuda_rc(launch_topk_sort_gather(LL.sx, LL.Lx, px, st, true));
+        } else {
+            rc = cuda_rc(launch_topk(LL.sx, LL.Lx, px, st));
+            if (!rc) rc = cuda_rc(launch_sort_gather(LL.sx, LL.Lx, px, st));
         }
-        dense(K_SHARED_DOWN, w + LL.hs, w_sd, ls.SI, ls.H, out, DENSE_F32_ADD);
+    }
+    if (!rc) rc = cuda_rc(launch_experts(LL.sx, LL.Lx, px, st));
+    if (!rc) rc = cuda_rc(launch_combine(LL.sx, LL.Lx, px, st));
+    if (!rc) {
+        timing_begin(K_LATENT_MID, st);
+        rc = cuda_rc(launch_latent_mid((const float*)(w + LL.yl), ln_w, ls.norm_eps, S, ls.LAT,
+                                       (__nv_bfloat16*)(w + LL.zl), (const float*)(w + LL.gu), ls.SI,
+                                       (__nv_bfloat16*)(w + LL.hs), st));
+        timing_end(st);
+    }
+    if (!rc) {
+        timing_begin(K_LATENT_UP, st);
+        rc = shared ? cuda_rc(launch_dense_kcat(w + LL.zl, w_up, ls.LAT, w + LL.hs, w_sd, ls.SI, S, ls.H, out,
+                                                DENSE_F32, sb, st, K_LATENT_UP))
+                    : cuda_rc(launch_dense(w + LL.zl, w_up, S, ls.LAT, ls.H, nullptr, out, DENSE_F32, sb, st,
+                                           K_LATENT_UP));
+        timing_end(st);
     }
     return rc;
 }

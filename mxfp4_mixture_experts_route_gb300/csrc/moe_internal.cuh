@@ -121,7 +121,7 @@ cudaError_t launch_pdl(void (*kern)(KArgs...), dim3 grid, dim3 block, size_t sme
 // ---------------------------------------------------------------------------
 enum KernelId {
     K_ROUTER = 0, K_TOPK, K_SORT, K_GATHER, K_EXPERTS, K_COMBINE, K_ROUTE_GATHER,
-    K_LATENT_DOWN, K_LATENT_NORM, K_LATENT_UP, K_SHARED_GU, K_SHARED_ACT, K_SHARED_DOWN, K_NUM
+    K_LATENT_DOWN, K_LATENT_MID, K_LATENT_UP, K_NUM
 };
 void timing_begin(int kernel_id, cudaStream_t st);
 void timing_end(cudaStream_t st);
@@ -190,8 +190,15 @@ cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& 
 // the stream's earlier kernels wrote) or bf16
 enum DenseOut { DENSE_F32 = 0, DENSE_F32_ADD = 1, DENSE_BF16 = 2 };
 bool dense_fits(int S, int K, int N);
+// (kt_id: the KernelId its diagnostics stamps go under)
 cudaError_t launch_dense(const void* x, const void* w, int S, int K, int N, const float* off, void* out, int mode,
-                         StatusBlock* sb, cudaStream_t st);
+                         StatusBlock* sb, cudaStream_t st, int kt_id);
+// two products in one launch: [x w^T | x w2^T] into out (N cols, mode) and
+// out2 (N2 cols, mode2); or x w^T + x2 w2^T (K and K2 long rows) into out
+cudaError_t launch_dense_ncat(const void* x, int S, int K, const void* w, int N, void* out, int mode, const void* w2,
+                              int N2, void* out2, int mode2, StatusBlock* sb, cudaStream_t st, int kt_id);
+cudaError_t launch_dense_kcat(const void* x, const void* w, int K, const void* x2, const void* w2, int K2, int S,
+                              int N, void* out, int mode, StatusBlock* sb, cudaStream_t st, int kt_id);
 cudaError_t launch_topk(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 // moe_forward at small S: top-k, sort and gather in one kernel (needs the
@@ -199,13 +206,18 @@ cudaError_t launch_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, c
 bool topk_sort_fits(const moe_shape& s);
 // ... and the fused kernel selects the top k itself (no top-k kernel before it)
 bool route_gather_selects(const moe_shape& s);
-cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+// (x_after_wait: the rows to gather were written by an earlier kernel of the
+// call, not an input of it)
+cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st,
+                                    bool x_after_wait = false);
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 // the latent-MoE layer's elementwise steps (latent.cu)
-cudaError_t launch_latent_norm(const float* yl, const float* ln_w, float eps, int S, int n, __nv_bfloat16* zl,
-                               cudaStream_t st);
-cudaError_t launch_shared_act(const float* gu, int S, int si, __nv_bfloat16* hs, cudaStream_t st);
+// zl = bf16(RMSNorm(yl) ln_w) and, when si > 0, hs = bf16(silu(g) u) of the
+// shared expert's gate/up rows gu, in one launch (n <= 16384, n % 4 == 0)
+bool latent_mid_fits(int n);
+cudaError_t launch_latent_mid(const float* yl, const float* ln_w, float eps, int S, int n, __nv_bfloat16* zl,
+                              const float* gu, int si, __nv_bfloat16* hs, cudaStream_t st);
 
 }  // namespace moe

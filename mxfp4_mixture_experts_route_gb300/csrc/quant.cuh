@@ -24,11 +24,10 @@ struct QuantChunk {
     int e;
 };
 
-// Elements 8c .. 8c+7 of the row `in` (d / 8 chunks).  All 32 lanes of the
-// warp call it (the block maximum is taken across lanes); act = c < d / 8
-// (whole blocks of four threads, d / 8 being a multiple of 16).
-__device__ __forceinline__ QuantChunk quantize_chunk(const uint4* __restrict__ in, int c, bool act) {
-    const uint4 v = act ? __ldg(in + c) : make_uint4(0, 0, 0, 0);
+// Eight bf16 elements v of one row (a thread's chunk).  All 32 lanes of the
+// warp call it (the block maximum is taken across lanes); lanes past the row
+// pass zeros (whole blocks of four threads, d / 8 being a multiple of 16).
+__device__ __forceinline__ QuantChunk quantize_vals(const uint4 v) {
     const uint32_t wv[4] = {v.x, v.y, v.z, v.w};
     float f[8];
 #pragma unroll
@@ -60,6 +59,17 @@ __device__ __forceinline__ QuantChunk quantize_chunk(const uint4* __restrict__ i
     q.lo = make_uint2(lw[0], lw[1]);
     q.e = e;
     return q;
+}
+
+// Elements 8c .. 8c+7 of the row `in` (d / 8 chunks; act = c < d / 8), an
+// input of the call (read through the read-only path)
+__device__ __forceinline__ QuantChunk quantize_chunk(const uint4* __restrict__ in, int c, bool act) {
+    return quantize_vals(act ? __ldg(in + c) : make_uint4(0, 0, 0, 0));
+}
+
+// The same for a row an earlier kernel of the call wrote (read through L2)
+__device__ __forceinline__ QuantChunk quantize_chunk_dep(const uint4* in, int c, bool act) {
+    return quantize_vals(act ? ld_dep(in + c) : make_uint4(0, 0, 0, 0));
 }
 
 // Chunk c of pick row r: its hi and lo bytes, and (first thread of the block)

@@ -19,6 +19,7 @@
 
 #include <cooperative_groups.h>
 #include <cudaTypedefs.h>
+#include <climits>
 
 namespace cg = cooperative_groups;
 
@@ -48,6 +49,14 @@ struct DCfg {
     static_assert(RS * R_STAGE >= RM * RN * 4, "the partial tile reuses the stage ring");
 };
 
+// A second product in the same launch: concatenated along N (tiles from
+// n_split on multiply the same x by w2 into out2, rows of N2) or along K
+// (slabs from k_split on take x2 and w2, into the same out).  INT_MAX: none.
+struct DenseTail {
+    void* out2;
+    int n_split, k_split, N2, mode2;
+};
+
 // out[t, n] = sum_k x[t, k] * w[n, k]: x [S, K] bf16, w [N, K] bf16, fp32
 // accumulation in TMEM.  grid (N / 128, ceil(S / RN), kslices) in clusters of
 // (1, 1, kslices) over K.  The weight slabs of the first stages are issued
@@ -56,8 +65,9 @@ struct DCfg {
 template <int RN>
 __global__ void __launch_bounds__(R_THREADS, 1)
     k_dense_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
+               const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x2,
                const float* __restrict__ off, void* out, int S, int K, int N, int kslices, int mode,
-               int w_evict_first, StatusBlock* __restrict__ sb) {
+               int w_evict_first, StatusBlock* __restrict__ sb, int kt_id, const DenseTail tail) {
     using C = DCfg<RN>;
     constexpr int RS = C::RS, R_STAGE = C::R_STAGE;
     extern __shared__ uint8_t smem_raw[];
@@ -70,7 +80,13 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     float* part = reinterpret_cast<float*>(sm);   // [RN][RM] partial products, after the MMAs
 
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+    KT_MARK(kt_id, 0);
     const int e0 = blockIdx.x * RM, t0 = blockIdx.y * RN, ks = blockIdx.z;
+    const bool part2 = (int)blockIdx.x >= tail.n_split;    // a tile of the second product (N-concatenation)
+    const int row0 = part2 ? e0 - tail.n_split * RM : e0;   // its first row in its own weights
+    // the weight map of slab k, and its slab within that map
+    auto wmap = [&](int k) { return (part2 || k >= tail.k_split) ? &tm_w2 : &tm_w; };
+    auto wslab = [&](int k) { return k >= tail.k_split ? k - tail.k_split : k; };
     const int nk = K / RK;
     const int kb = (int)((long long)nk * ks / kslices), ke = (int)((long long)nk * (ks + 1) / kslices);
     if (threadIdx.x == 0) {
@@ -88,6 +104,10 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tm_w);
         ptx::prefetch_tensormap(&tm_x);
+        if (tail.n_split != INT_MAX || tail.k_split != INT_MAX) {
+            ptx::prefetch_tensormap(&tm_w2);
+            ptx::prefetch_tensormap(&tm_x2);
+        }
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -97,11 +117,12 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     if (warp == 0 && lane == 0) {
         for (int i = 0; i < n_pre; ++i) {
             ptx::mbar_arrive_expect_tx(&full[i], R_STAGE);
-            ptx::tma_load_2d(sm + i * R_STAGE, &tm_w, (kb + i) * RK, e0, &full[i], pol_w);
+            ptx::tma_load_2d(sm + i * R_STAGE, wmap(kb + i), wslab(kb + i) * RK, row0, &full[i], pol_w);
         }
     }
     pdl_wait();      // x may come from the stream's previous kernel
     pdl_trigger();   // successors start once this kernel's inputs are final
+    KT_MARK(kt_id, 1);
 
     auto fail = [&](int site) {
         latch_status(sb, MOE_ERR_TIMEOUT, 100 + site);
@@ -118,9 +139,9 @@ __global__ void __launch_bounds__(R_THREADS, 1)
                         break;
                     }
                     ptx::mbar_arrive_expect_tx(&full[s], R_STAGE);
-                    ptx::tma_load_2d(st, &tm_w, k * RK, e0, &full[s], pol_w);
+                    ptx::tma_load_2d(st, wmap(k), wslab(k) * RK, row0, &full[s], pol_w);
                 }
-                ptx::tma_load_2d(st + R_A, &tm_x, k * RK, t0, &full[s], pol_x);
+                ptx::tma_load_2d(st + R_A, k >= tail.k_split ? &tm_x2 : &tm_x, wslab(k) * RK, t0, &full[s], pol_x);
             }
         }
     } else if (warp == 1) {
@@ -147,6 +168,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
         const int q = warp & 3;
         const int m = 32 * q + lane;
         const bool got = ptx::mbar_wait_warp(done, 0, abort_flag, R_WAIT_NS);
+        if (warp == 2) KT_MARK(kt_id, 4);
         if (!got && lane == 0) fail(3);
         if (got) {
             ptx::tc_fence_after();
@@ -166,6 +188,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     // writes tokens [r RN / KS, (r + 1) RN / KS) of the tile
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
+    KT_MARK(kt_id, 5);
     if (!*abort_flag) {
         const int n0 = RN * ks / kslices, n1 = RN * (ks + 1) / kslices;
         for (int idx = threadIdx.x; idx < (n1 - n0) * RM; idx += R_THREADS) {
@@ -177,46 +200,81 @@ __global__ void __launch_bounds__(R_THREADS, 1)
             float z = 0.f;
 #pragma unroll
             for (int r = 0; r < R_MAX_CLUSTER; ++r) z += pz[r];
-            const int t = t0 + n, e = e0 + mm;
-            if (t < S && e < N) {
-                const size_t o = (size_t)t * N + e;
-                if (mode == DENSE_BF16) {
-                    reinterpret_cast<__nv_bfloat16*>(out)[o] = __float2bfloat16_rn(z);
-                } else if (mode == DENSE_F32_ADD) {
-                    float* of = reinterpret_cast<float*>(out);
+            const int t = t0 + n, e = row0 + mm;
+            const int width = part2 ? tail.N2 : N, md = part2 ? tail.mode2 : mode;
+            void* dst = part2 ? tail.out2 : out;
+            if (t < S && e < width) {
+                const size_t o = (size_t)t * width + e;
+                if (md == DENSE_BF16) {
+                    reinterpret_cast<__nv_bfloat16*>(dst)[o] = __float2bfloat16_rn(z);
+                } else if (md == DENSE_F32_ADD) {
+                    float* of = reinterpret_cast<float*>(dst);
                     of[o] = ld_dep(of + o) + z;
                 } else {
-                    reinterpret_cast<float*>(out)[o] = off ? z + off[e] : z;
+                    reinterpret_cast<float*>(dst)[o] = (off && !part2) ? z + off[e] : z;
                 }
             }
         }
     }
     cluster.sync();   // every CTA keeps its partial tile until the others have read it
+    KT_MARK(kt_id, 2);
     ptx::tc_fence_after();
     if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
+// One launch of k_dense_tc<RN> over [w; w2] (N-concatenation: N2 > 0) or
+// [x, x2] . [w, w2] (K-concatenation: K2 > 0), or w alone.
+struct DenseArgs {
+    const void *x, *w, *x2, *w2;
+    int S, K, N, K2, N2;
+    const float* off;
+    void *out, *out2;
+    int mode, mode2;
+};
+
 template <int RN>
-cudaError_t launch_dense_rn(const void* x, const void* w, int S, int K, int N, const float* off, void* out,
-                            int mode, bool w_once, StatusBlock* sb, cudaStream_t st) {
+cudaError_t launch_dense_rn(const DenseArgs& d, bool w_once, StatusBlock* sb, cudaStream_t st, int kt_id) {
     using C = DCfg<RN>;
-    CUtensorMap tm_w, tm_x;
-    const uint64_t w_d[2] = {(uint64_t)K, (uint64_t)N}, w_s[1] = {(uint64_t)K * 2};
-    const uint64_t x_d[2] = {(uint64_t)K, (uint64_t)S}, x_s[1] = {(uint64_t)K * 2};
+    KT_BIND();
+    CUtensorMap tm_w, tm_x, tm_w2, tm_x2;
+    const int Kx = d.K, Kw2 = d.K2 > 0 ? d.K2 : d.K;   // row lengths of x / w and of x2 / w2
+    const uint64_t w_d[2] = {(uint64_t)Kx, (uint64_t)d.N}, w_s[1] = {(uint64_t)Kx * 2};
+    const uint64_t x_d[2] = {(uint64_t)Kx, (uint64_t)d.S}, x_s[1] = {(uint64_t)Kx * 2};
     const uint32_t w_b[2] = {RK, RM}, x_b[2] = {RK, RN};
-    if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, w, 2, w_d, w_s, w_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, x, 2, x_d, x_s, x_b, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.w, 2, w_d, w_s, w_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
+        !make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.x, 2, x_d, x_s, x_b, CU_TENSOR_MAP_SWIZZLE_128B))
         return cudaErrorInvalidValue;
-    const int tiles = (N / RM) * ((S + RN - 1) / RN);
-    const int nk = K / RK;
+    tm_w2 = tm_w;
+    tm_x2 = tm_x;
+    if (d.N2 > 0 || d.K2 > 0) {
+        const int N2rows = d.N2 > 0 ? d.N2 : d.N;
+        const uint64_t w2_d[2] = {(uint64_t)Kw2, (uint64_t)N2rows}, w2_s[1] = {(uint64_t)Kw2 * 2};
+        if (!make_map(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.w2, 2, w2_d, w2_s, w_b, CU_TENSOR_MAP_SWIZZLE_128B))
+            return cudaErrorInvalidValue;
+        if (d.K2 > 0) {
+            const uint64_t x2_d[2] = {(uint64_t)d.K2, (uint64_t)d.S}, x2_s[1] = {(uint64_t)d.K2 * 2};
+            if (!make_map(&tm_x2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.x2, 2, x2_d, x2_s, x_b,
+                          CU_TENSOR_MAP_SWIZZLE_128B))
+                return cudaErrorInvalidValue;
+        }
+    }
+    const int ntile = (d.N + (d.N2 > 0 ? d.N2 : 0)) / RM;
+    const int tiles = ntile * ((d.S + RN - 1) / RN);
+    const int nk = (d.K + (d.K2 > 0 ? d.K2 : 0)) / RK;
     int ks = num_sms() / tiles;                 // at most one CTA per SM: a second wave would double the time
     if (ks > R_MAX_CLUSTER) ks = R_MAX_CLUSTER;
     if (ks > nk / 4) ks = nk / 4;               // at least four slabs per CTA
     if (ks < 1) ks = 1;
+    DenseTail tail;
+    tail.out2 = d.out2;
+    tail.n_split = d.N2 > 0 ? d.N / RM : INT_MAX;
+    tail.k_split = d.K2 > 0 ? d.K / RK : INT_MAX;
+    tail.N2 = d.N2;
+    tail.mode2 = d.mode2;
     cudaError_t e = cudaFuncSetAttribute(k_dense_tc<RN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
-    cfg.gridDim = dim3(N / RM, (S + RN - 1) / RN, ks);
+    cfg.gridDim = dim3(ntile, (d.S + RN - 1) / RN, ks);
     cfg.blockDim = dim3(R_THREADS);
     cfg.dynamicSmemBytes = C::SMEM;
     cfg.stream = st;
@@ -229,7 +287,15 @@ cudaError_t launch_dense_rn(const void* x, const void* w, int S, int K, int N, c
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_dense_tc<RN>, tm_w, tm_x, off, out, S, K, N, ks, mode, w_once ? 1 : 0, sb);
+    return cudaLaunchKernelEx(&cfg, k_dense_tc<RN>, tm_w, tm_x, tm_w2, tm_x2, d.off, d.out, d.S, nk * RK, d.N, ks,
+                              d.mode, w_once ? 1 : 0, sb, kt_id, tail);
+}
+
+cudaError_t launch_dense_args(const DenseArgs& d, StatusBlock* sb, cudaStream_t st, int kt_id) {
+    // one token tile of 16 for up to 16 tokens (a weight-streaming product), else tiles of 128; the
+    // weights are read once (evict first) unless several token tiles read them
+    if (d.S <= 16) return launch_dense_rn<16>(d, true, sb, st, kt_id);
+    return launch_dense_rn<128>(d, d.S <= 128, sb, st, kt_id);
 }
 
 }  // namespace
@@ -239,16 +305,27 @@ bool router_tc_fits(const moe_shape& s) { return s.S >= 64 && s.E % RM == 0 && s
 bool dense_fits(int S, int K, int N) { return S >= 1 && N % RM == 0 && K % RK == 0 && K / RK >= 1; }
 
 cudaError_t launch_dense(const void* x, const void* w, int S, int K, int N, const float* off, void* out, int mode,
-                         StatusBlock* sb, cudaStream_t st) {
-    // one token tile of 16 for up to 16 tokens (a weight-streaming product), else tiles of 128; the
-    // weights are read once (evict first) unless several token tiles read them
-    if (S <= 16) return launch_dense_rn<16>(x, w, S, K, N, off, out, mode, true, sb, st);
-    return launch_dense_rn<128>(x, w, S, K, N, off, out, mode, S <= 128, sb, st);
+                         StatusBlock* sb, cudaStream_t st, int kt_id) {
+    const DenseArgs d{x, w, nullptr, nullptr, S, K, N, 0, 0, off, out, nullptr, mode, 0};
+    return launch_dense_args(d, sb, st, kt_id);
+}
+
+cudaError_t launch_dense_ncat(const void* x, int S, int K, const void* w, int N, void* out, int mode, const void* w2,
+                              int N2, void* out2, int mode2, StatusBlock* sb, cudaStream_t st, int kt_id) {
+    const DenseArgs d{x, w, nullptr, w2, S, K, N, 0, N2, nullptr, out, out2, mode, mode2};
+    return launch_dense_args(d, sb, st, kt_id);
+}
+
+cudaError_t launch_dense_kcat(const void* x, const void* w, int K, const void* x2, const void* w2, int K2, int S,
+                              int N, void* out, int mode, StatusBlock* sb, cudaStream_t st, int kt_id) {
+    const DenseArgs d{x, w, x2, w2, S, K, N, K2, 0, nullptr, out, nullptr, mode, 0};
+    return launch_dense_args(d, sb, st, kt_id);
 }
 
 cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    return launch_dense_rn<128>(p.x, p.w_gate, s.S, s.d, s.E, p.logit_off, p.ws + L.logits, DENSE_F32, false,
-                                reinterpret_cast<StatusBlock*>(p.ws + L.status), st);
+    const DenseArgs d{p.x, p.w_gate, nullptr, nullptr, s.S, s.d, s.E, 0, 0, p.logit_off, p.ws + L.logits, nullptr,
+                      DENSE_F32, 0};
+    return launch_dense_rn<128>(d, false, reinterpret_cast<StatusBlock*>(p.ws + L.status), st, K_ROUTER);
 }
 
 }  // namespace moe

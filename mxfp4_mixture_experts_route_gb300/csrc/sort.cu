@@ -325,7 +325,9 @@ __global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __re
 // token t's row (quantised before the wait) at r_p; CTA 0 writes the counts.
 // The picks of a token are distinct valid experts.  With FROM_IDS the ids
 // come from the top-k kernel instead (more tokens than each CTA should select
-// again): every CTA reads them and only places and gathers.
+// again): every CTA reads them and only places and gathers.  The rows are
+// quantised before the wait when they are an input of the call, after it
+// when an earlier kernel of the call wrote them (x_after_wait).
 constexpr int RG_THREADS = 512;        // at most; 16 warps: two tokens a warp at S = 32
 constexpr int RG_PASSES = 4;           // chunks of 8 elements a thread, at most: d <= 16384
 constexpr int RG_TOKENS_PER_WARP = 2;
@@ -335,7 +337,8 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
                                                             int k, int d, int I, int P_tab,
                                                             int32_t* __restrict__ ids, float* __restrict__ weights,
                                                             SortOut o, uint8_t* __restrict__ xq,
-                                                            uint8_t* __restrict__ xs, uint8_t* __restrict__ hs) {
+                                                            uint8_t* __restrict__ xs, uint8_t* __restrict__ hs,
+                                                            int x_after_wait) {
     extern __shared__ int32_t smem[];
     KT_MARK(K_ROUTE_GATHER, 0);
     pdl_trigger();
@@ -349,16 +352,25 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     const int nc = d / 8;
     QuantChunk q[PASSES];
+    if (!x_after_wait) {
 #pragma unroll
-    for (int i = 0; i < PASSES; ++i) {
-        const int c = i * (int)blockDim.x + tid;
-        if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, c, c < nc);   // block-uniform condition
+        for (int i = 0; i < PASSES; ++i) {
+            const int c = i * (int)blockDim.x + tid;
+            if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, c, c < nc);   // block-uniform condition
+        }
     }
     float b[MAXE];
     if constexpr (!FROM_IDS) load_bias(bias, E, lane, b);
     for (int i = tid; i < E; i += blockDim.x) cnt[i] = 0;
     pdl_wait();
     KT_MARK(K_ROUTE_GATHER, 1);
+    if (x_after_wait) {
+#pragma unroll
+        for (int i = 0; i < PASSES; ++i) {
+            const int c = i * (int)blockDim.x + tid;
+            if (i * (int)blockDim.x < nc) q[i] = quantize_chunk_dep(in, c, c < nc);
+        }
+    }
     if constexpr (FROM_IDS) {
         for (int i = tid; i < P; i += blockDim.x) key[i] = ld_dep(ids + i);
     } else {
@@ -505,7 +517,7 @@ static int route_gather_threads(const moe_shape& s) {
 }
 
 template <int MAXE, bool FROM_IDS>
-static cudaError_t launch_rg(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+static cudaError_t launch_rg(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st, bool x_after_wait) {
     const int threads = route_gather_threads(s);
     const int P = s.S * s.k;
     const size_t smem = (size_t)(P + s.E) * sizeof(int32_t) +
@@ -520,19 +532,20 @@ static cudaError_t launch_rg(const moe_shape& s, const WsLayout& L, const Ptrs& 
     e = launch_pdl(kern, dim3(P), dim3(threads), smem, st, reinterpret_cast<const float*>(ws + L.logits), p.bias,
                    p.x, s.S, s.E, s.k, s.d, s.I, L.max_picks, p.ids, p.weights, sort_out(L, ws),
                    reinterpret_cast<uint8_t*>(ws + L.xq), reinterpret_cast<uint8_t*>(ws + L.xs),
-                   reinterpret_cast<uint8_t*>(ws + L.hs));
+                   reinterpret_cast<uint8_t*>(ws + L.hs), x_after_wait ? 1 : 0);
     timing_end(st);
     return e;
 }
 
-cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st,
+                                    bool x_after_wait) {
     KT_BIND();
     if (!route_gather_selects(s)) {
         cudaError_t e = launch_topk(s, L, p, st);
         if (e != cudaSuccess) return e;
-        return launch_rg<8, true>(s, L, p, st);
+        return launch_rg<8, true>(s, L, p, st, x_after_wait);
     }
-    return s.E <= 256 ? launch_rg<8, false>(s, L, p, st) : launch_rg<16, false>(s, L, p, st);
+    return s.E <= 256 ? launch_rg<8, false>(s, L, p, st, x_after_wait) : launch_rg<16, false>(s, L, p, st, x_after_wait);
 }
 
 }  // namespace moe

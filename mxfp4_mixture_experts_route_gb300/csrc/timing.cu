@@ -18,8 +18,7 @@ int g_used = 0;            // pairs recorded since the last collect
 int g_open = -1;           // pair started by timing_begin, not yet ended
 
 const char* const kNames[K_NUM] = {"router_logits", "topk", "sort", "gather", "experts", "combine", "topk_sort_gather",
-                                   "latent_down", "latent_norm", "latent_up", "shared_gate_up", "shared_act",
-                                   "shared_down"};
+                                   "latent_down", "latent_mid", "latent_up"};
 
 void free_all() {
     for (auto& r : g_recs) {
