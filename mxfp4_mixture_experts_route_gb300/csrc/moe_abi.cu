@@ -427,15 +427,17 @@ int moe_latent_forward(const moe_latent_shape* shape, const void* x, const void*
     char* w = (char*)ws;
     StatusBlock* sb = reinterpret_cast<StatusBlock*>(w + LL.Lr.status);
     const int S = ls.S;
-    // k2 page, K2b's stages, in seven launches at small S:
-    //   1. the router's logits over the layer input x (over H)
-    //   2. latent down xl = bf16(x . w_ld^T) and the shared expert's gate/up
-    //      gu = x . w_sgu^T, one launch (the same x, the weights one after the other)
-    //   3. top-k, sort and gather of xl (the block's workspace over LAT shares
+    // k2 page, K2b's stages, in six launches at small S:
+    //   1. the router's logits L = x . w_gate^T (+ offset), latent down
+    //      xl = bf16(x . w_ld^T) and the shared expert's gate/up gu = x . w_sgu^T,
+    //      one launch (products of the same x over H, the weights one after
+    //      the other along N; the router in its own kernel before it when E is
+    //      not a multiple of 128)
+    //   2. top-k, sort and gather of xl (the block's workspace over LAT shares
     //      the router's status, logits, pos and tile regions)
-    //   4-5. the expert GEMMs and the combine: yl
-    //   6. zl = bf16(RMSNorm(yl) ln_w) and hs = bf16(silu(g) u)
-    //   7. out = zl . w_up^T + hs . w_sd^T, one launch (the two products
+    //   3-4. the expert GEMMs and the combine: yl
+    //   5. zl = bf16(RMSNorm(yl) ln_w) and hs = bf16(silu(g) u)
+    //   6. out = zl . w_up^T + hs . w_sd^T, one launch (the two products
     //      concatenated along K)
     Ptrs pr{};
     pr.x = (const __nv_bfloat16*)x;
@@ -445,13 +447,19 @@ int moe_latent_forward(const moe_latent_shape* shape, const void* x, const void*
     pr.ids = ids;
     pr.weights = weights;
     pr.ws = w;
-    rc = cuda_rc(launch_router_logits(LL.sr, LL.Lr, pr, st));
+    // the router's logits join the latent-down launch as its first part when
+    // its experts fill whole 128-row tiles; otherwise the router's own kernel
+    const bool router_part = ls.E % 128 == 0;
+    if (!router_part) rc = cuda_rc(launch_router_logits(LL.sr, LL.Lr, pr, st));
     if (!rc) {
+        DensePart parts[3];
+        int np = 0;
+        if (router_part) parts[np++] = DensePart{w_gate, ls.E, w + LL.Lr.logits, DENSE_F32};
+        parts[np++] = DensePart{w_ld, ls.LAT, w + LL.xl, DENSE_BF16};
+        if (shared) parts[np++] = DensePart{w_sgu, 2 * ls.SI, w + LL.gu, DENSE_F32};
         timing_begin(K_LATENT_DOWN, st);
-        rc = shared ? cuda_rc(launch_dense_ncat(x, S, ls.H, w_ld, ls.LAT, w + LL.xl, DENSE_BF16, w_sgu, 2 * ls.SI,
-                                                w + LL.gu, DENSE_F32, sb, st, K_LATENT_DOWN))
-                    : cuda_rc(launch_dense(x, w_ld, S, ls.H, ls.LAT, nullptr, w + LL.xl, DENSE_BF16, sb, st,
-                                           K_LATENT_DOWN));
+        rc = cuda_rc(launch_dense_ncat(x, S, ls.H, parts, np, router_part ? pr.logit_off : nullptr, sb, st,
+                                       K_LATENT_DOWN));
         timing_end(st);
     }
     Ptrs px{};

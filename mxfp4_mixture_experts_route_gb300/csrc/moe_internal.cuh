@@ -193,10 +193,17 @@ bool dense_fits(int S, int K, int N);
 // (kt_id: the KernelId its diagnostics stamps go under)
 cudaError_t launch_dense(const void* x, const void* w, int S, int K, int N, const float* off, void* out, int mode,
                          StatusBlock* sb, cudaStream_t st, int kt_id);
-// two products in one launch: [x w^T | x w2^T] into out (N cols, mode) and
-// out2 (N2 cols, mode2); or x w^T + x2 w2^T (K and K2 long rows) into out
-cudaError_t launch_dense_ncat(const void* x, int S, int K, const void* w, int N, void* out, int mode, const void* w2,
-                              int N2, void* out2, int mode2, StatusBlock* sb, cudaStream_t st, int kt_id);
+// up to three products of the same x in one launch: part i = x . w^T into
+// out (N cols a token, mode), the logit offset added to part 0's; or
+// x . w^T + x2 . w2^T (K and K2 long rows) into one out
+struct DensePart {
+    const void* w;
+    int N;
+    void* out;
+    int mode;
+};
+cudaError_t launch_dense_ncat(const void* x, int S, int K, const DensePart* p, int n_parts, const float* off,
+                              StatusBlock* sb, cudaStream_t st, int kt_id);
 cudaError_t launch_dense_kcat(const void* x, const void* w, int K, const void* x2, const void* w2, int K2, int S,
                               int N, void* out, int mode, StatusBlock* sb, cudaStream_t st, int kt_id);
 cudaError_t launch_topk(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);

@@ -49,12 +49,15 @@ struct DCfg {
     static_assert(RS * R_STAGE >= RM * RN * 4, "the partial tile reuses the stage ring");
 };
 
-// A second product in the same launch: concatenated along N (tiles from
-// n_split on multiply the same x by w2 into out2, rows of N2) or along K
-// (slabs from k_split on take x2 and w2, into the same out).  INT_MAX: none.
-struct DenseTail {
-    void* out2;
-    int n_split, k_split, N2, mode2;
+// Up to three products of the same x in one launch, concatenated along N:
+// part i (weights w, w2, w3) starts at tile tile0[i] (INT_MAX: absent) and
+// writes its rows to out[i] (width[i] columns a token, mode[i]); or two
+// products into one output concatenated along K: slabs from k_split on take
+// x2 and w2 (INT_MAX: none).  The logit offset applies to part 0.
+struct DenseParts {
+    void* out[3];
+    int tile0[3], width[3], mode[3];
+    int k_split;
 };
 
 // out[t, n] = sum_k x[t, k] * w[n, k]: x [S, K] bf16, w [N, K] bf16, fp32
@@ -66,8 +69,8 @@ template <int RN>
 __global__ void __launch_bounds__(R_THREADS, 1)
     k_dense_tc(const __grid_constant__ CUtensorMap tm_w, const __grid_constant__ CUtensorMap tm_x,
                const __grid_constant__ CUtensorMap tm_w2, const __grid_constant__ CUtensorMap tm_x2,
-               const float* __restrict__ off, void* out, int S, int K, int N, int kslices, int mode,
-               int w_evict_first, StatusBlock* __restrict__ sb, int kt_id, const DenseTail tail) {
+               const __grid_constant__ CUtensorMap tm_w3, const float* __restrict__ off, int S, int K, int kslices,
+               int w_evict_first, StatusBlock* __restrict__ sb, int kt_id, const DenseParts parts) {
     using C = DCfg<RN>;
     constexpr int RS = C::RS, R_STAGE = C::R_STAGE;
     extern __shared__ uint8_t smem_raw[];
@@ -82,11 +85,14 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
     KT_MARK(kt_id, 0);
     const int e0 = blockIdx.x * RM, t0 = blockIdx.y * RN, ks = blockIdx.z;
-    const bool part2 = (int)blockIdx.x >= tail.n_split;    // a tile of the second product (N-concatenation)
-    const int row0 = part2 ? e0 - tail.n_split * RM : e0;   // its first row in its own weights
+    const int bx = (int)blockIdx.x;
+    const int pidx = bx >= parts.tile0[2] ? 2 : bx >= parts.tile0[1] ? 1 : 0;   // the tile's product
+    const int row0 = e0 - parts.tile0[pidx] * RM;                               // its first row in its weights
     // the weight map of slab k, and its slab within that map
-    auto wmap = [&](int k) { return (part2 || k >= tail.k_split) ? &tm_w2 : &tm_w; };
-    auto wslab = [&](int k) { return k >= tail.k_split ? k - tail.k_split : k; };
+    auto wmap = [&](int k) {
+        return pidx == 2 ? &tm_w3 : (pidx == 1 || k >= parts.k_split) ? &tm_w2 : &tm_w;
+    };
+    auto wslab = [&](int k) { return k >= parts.k_split ? k - parts.k_split : k; };
     const int nk = K / RK;
     const int kb = (int)((long long)nk * ks / kslices), ke = (int)((long long)nk * (ks + 1) / kslices);
     if (threadIdx.x == 0) {
@@ -104,10 +110,9 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tensormap(&tm_w);
         ptx::prefetch_tensormap(&tm_x);
-        if (tail.n_split != INT_MAX || tail.k_split != INT_MAX) {
-            ptx::prefetch_tensormap(&tm_w2);
-            ptx::prefetch_tensormap(&tm_x2);
-        }
+        if (pidx == 1 || parts.k_split != INT_MAX) ptx::prefetch_tensormap(&tm_w2);
+        if (parts.k_split != INT_MAX) ptx::prefetch_tensormap(&tm_x2);
+        if (pidx == 2) ptx::prefetch_tensormap(&tm_w3);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -141,7 +146,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
                     ptx::mbar_arrive_expect_tx(&full[s], R_STAGE);
                     ptx::tma_load_2d(st, wmap(k), wslab(k) * RK, row0, &full[s], pol_w);
                 }
-                ptx::tma_load_2d(st + R_A, k >= tail.k_split ? &tm_x2 : &tm_x, wslab(k) * RK, t0, &full[s], pol_x);
+                ptx::tma_load_2d(st + R_A, k >= parts.k_split ? &tm_x2 : &tm_x, wslab(k) * RK, t0, &full[s], pol_x);
             }
         }
     } else if (warp == 1) {
@@ -201,8 +206,8 @@ __global__ void __launch_bounds__(R_THREADS, 1)
 #pragma unroll
             for (int r = 0; r < R_MAX_CLUSTER; ++r) z += pz[r];
             const int t = t0 + n, e = row0 + mm;
-            const int width = part2 ? tail.N2 : N, md = part2 ? tail.mode2 : mode;
-            void* dst = part2 ? tail.out2 : out;
+            const int width = parts.width[pidx], md = parts.mode[pidx];
+            void* dst = parts.out[pidx];
             if (t < S && e < width) {
                 const size_t o = (size_t)t * width + e;
                 if (md == DENSE_BF16) {
@@ -211,7 +216,7 @@ __global__ void __launch_bounds__(R_THREADS, 1)
                     float* of = reinterpret_cast<float*>(dst);
                     of[o] = ld_dep(of + o) + z;
                 } else {
-                    reinterpret_cast<float*>(dst)[o] = (off && !part2) ? z + off[e] : z;
+                    reinterpret_cast<float*>(dst)[o] = (off && pidx == 0) ? z + off[e] : z;
                 }
             }
         }
@@ -222,55 +227,58 @@ __global__ void __launch_bounds__(R_THREADS, 1)
     if (warp == 1) ptx::tmem_dealloc(tmem, C::TMEM_COLS);
 }
 
-// One launch of k_dense_tc<RN> over [w; w2] (N-concatenation: N2 > 0) or
-// [x, x2] . [w, w2] (K-concatenation: K2 > 0), or w alone.
+// One launch of k_dense_tc<RN>: x [S, K] times the parts' weights (N-
+// concatenation: w[i] [N[i], K], N[i] = 0 for an absent part), or
+// x . w^T + x2 . w2^T (K-concatenation: K2 > 0, w [N, K], w2 [N, K2],
+// x2 [S, K2]).
 struct DenseArgs {
-    const void *x, *w, *x2, *w2;
-    int S, K, N, K2, N2;
+    const void* x;
+    const void* x2;
+    const void* w[3];
+    int S, K, K2;
+    int N[3];
     const float* off;
-    void *out, *out2;
-    int mode, mode2;
+    void* out[3];
+    int mode[3];
 };
 
 template <int RN>
 cudaError_t launch_dense_rn(const DenseArgs& d, bool w_once, StatusBlock* sb, cudaStream_t st, int kt_id) {
     using C = DCfg<RN>;
     KT_BIND();
-    CUtensorMap tm_w, tm_x, tm_w2, tm_x2;
-    const int Kx = d.K, Kw2 = d.K2 > 0 ? d.K2 : d.K;   // row lengths of x / w and of x2 / w2
-    const uint64_t w_d[2] = {(uint64_t)Kx, (uint64_t)d.N}, w_s[1] = {(uint64_t)Kx * 2};
-    const uint64_t x_d[2] = {(uint64_t)Kx, (uint64_t)d.S}, x_s[1] = {(uint64_t)Kx * 2};
+    CUtensorMap tm[3], tm_x, tm_x2;
     const uint32_t w_b[2] = {RK, RM}, x_b[2] = {RK, RN};
-    if (!make_map(&tm_w, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.w, 2, w_d, w_s, w_b, CU_TENSOR_MAP_SWIZZLE_128B) ||
-        !make_map(&tm_x, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.x, 2, x_d, x_s, x_b, CU_TENSOR_MAP_SWIZZLE_128B))
-        return cudaErrorInvalidValue;
-    tm_w2 = tm_w;
+    auto map2d = [&](CUtensorMap* m, const void* base, int cols, int rows, const uint32_t* box) {
+        const uint64_t dims[2] = {(uint64_t)cols, (uint64_t)rows}, str[1] = {(uint64_t)cols * 2};
+        return make_map(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, base, 2, dims, str, box, CU_TENSOR_MAP_SWIZZLE_128B);
+    };
+    if (!map2d(&tm[0], d.w[0], d.K, d.N[0], w_b) || !map2d(&tm_x, d.x, d.K, d.S, x_b)) return cudaErrorInvalidValue;
+    tm[1] = tm[2] = tm[0];
     tm_x2 = tm_x;
-    if (d.N2 > 0 || d.K2 > 0) {
-        const int N2rows = d.N2 > 0 ? d.N2 : d.N;
-        const uint64_t w2_d[2] = {(uint64_t)Kw2, (uint64_t)N2rows}, w2_s[1] = {(uint64_t)Kw2 * 2};
-        if (!make_map(&tm_w2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.w2, 2, w2_d, w2_s, w_b, CU_TENSOR_MAP_SWIZZLE_128B))
+    if (d.K2 > 0) {
+        if (!map2d(&tm[1], d.w[1], d.K2, d.N[0], w_b) || !map2d(&tm_x2, d.x2, d.K2, d.S, x_b))
             return cudaErrorInvalidValue;
-        if (d.K2 > 0) {
-            const uint64_t x2_d[2] = {(uint64_t)d.K2, (uint64_t)d.S}, x2_s[1] = {(uint64_t)d.K2 * 2};
-            if (!make_map(&tm_x2, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, d.x2, 2, x2_d, x2_s, x_b,
-                          CU_TENSOR_MAP_SWIZZLE_128B))
-                return cudaErrorInvalidValue;
-        }
+    } else {
+        for (int i = 1; i < 3; ++i)
+            if (d.N[i] > 0 && !map2d(&tm[i], d.w[i], d.K, d.N[i], w_b)) return cudaErrorInvalidValue;
     }
-    const int ntile = (d.N + (d.N2 > 0 ? d.N2 : 0)) / RM;
+    DenseParts parts;
+    int ntile = 0;
+    for (int i = 0; i < 3; ++i) {
+        const bool on = i == 0 || (d.K2 == 0 && d.N[i] > 0);
+        parts.tile0[i] = on ? ntile : INT_MAX;
+        parts.out[i] = d.out[i];
+        parts.width[i] = d.N[i];
+        parts.mode[i] = d.mode[i];
+        if (on) ntile += d.N[i] / RM;
+    }
+    parts.k_split = d.K2 > 0 ? d.K / RK : INT_MAX;
     const int tiles = ntile * ((d.S + RN - 1) / RN);
     const int nk = (d.K + (d.K2 > 0 ? d.K2 : 0)) / RK;
     int ks = num_sms() / tiles;                 // at most one CTA per SM: a second wave would double the time
     if (ks > R_MAX_CLUSTER) ks = R_MAX_CLUSTER;
     if (ks > nk / 4) ks = nk / 4;               // at least four slabs per CTA
     if (ks < 1) ks = 1;
-    DenseTail tail;
-    tail.out2 = d.out2;
-    tail.n_split = d.N2 > 0 ? d.N / RM : INT_MAX;
-    tail.k_split = d.K2 > 0 ? d.K / RK : INT_MAX;
-    tail.N2 = d.N2;
-    tail.mode2 = d.mode2;
     cudaError_t e = cudaFuncSetAttribute(k_dense_tc<RN>, cudaFuncAttributeMaxDynamicSharedMemorySize, C::SMEM);
     if (e != cudaSuccess) return e;
     cudaLaunchConfig_t cfg = {};
@@ -287,8 +295,8 @@ cudaError_t launch_dense_rn(const DenseArgs& d, bool w_once, StatusBlock* sb, cu
     attr[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, k_dense_tc<RN>, tm_w, tm_x, tm_w2, tm_x2, d.off, d.out, d.S, nk * RK, d.N, ks,
-                              d.mode, w_once ? 1 : 0, sb, kt_id, tail);
+    return cudaLaunchKernelEx(&cfg, k_dense_tc<RN>, tm[0], tm_x, tm[1], tm_x2, tm[2], d.off, d.S, nk * RK, ks,
+                              w_once ? 1 : 0, sb, kt_id, parts);
 }
 
 cudaError_t launch_dense_args(const DenseArgs& d, StatusBlock* sb, cudaStream_t st, int kt_id) {
@@ -306,25 +314,33 @@ bool dense_fits(int S, int K, int N) { return S >= 1 && N % RM == 0 && K % RK ==
 
 cudaError_t launch_dense(const void* x, const void* w, int S, int K, int N, const float* off, void* out, int mode,
                          StatusBlock* sb, cudaStream_t st, int kt_id) {
-    const DenseArgs d{x, w, nullptr, nullptr, S, K, N, 0, 0, off, out, nullptr, mode, 0};
+    const DenseArgs d{x, nullptr, {w, nullptr, nullptr}, S, K, 0, {N, 0, 0}, off, {out, nullptr, nullptr},
+                      {mode, 0, 0}};
     return launch_dense_args(d, sb, st, kt_id);
 }
 
-cudaError_t launch_dense_ncat(const void* x, int S, int K, const void* w, int N, void* out, int mode, const void* w2,
-                              int N2, void* out2, int mode2, StatusBlock* sb, cudaStream_t st, int kt_id) {
-    const DenseArgs d{x, w, nullptr, w2, S, K, N, 0, N2, nullptr, out, out2, mode, mode2};
+cudaError_t launch_dense_ncat(const void* x, int S, int K, const DensePart* p, int n_parts, const float* off,
+                              StatusBlock* sb, cudaStream_t st, int kt_id) {
+    DenseArgs d{x, nullptr, {nullptr, nullptr, nullptr}, S, K, 0, {0, 0, 0}, off, {nullptr, nullptr, nullptr},
+                {0, 0, 0}};
+    for (int i = 0; i < n_parts && i < 3; ++i) {
+        d.w[i] = p[i].w;
+        d.N[i] = p[i].N;
+        d.out[i] = p[i].out;
+        d.mode[i] = p[i].mode;
+    }
     return launch_dense_args(d, sb, st, kt_id);
 }
 
 cudaError_t launch_dense_kcat(const void* x, const void* w, int K, const void* x2, const void* w2, int K2, int S,
                               int N, void* out, int mode, StatusBlock* sb, cudaStream_t st, int kt_id) {
-    const DenseArgs d{x, w, x2, w2, S, K, N, K2, 0, nullptr, out, nullptr, mode, 0};
+    const DenseArgs d{x, x2, {w, w2, nullptr}, S, K, K2, {N, 0, 0}, nullptr, {out, nullptr, nullptr}, {mode, 0, 0}};
     return launch_dense_args(d, sb, st, kt_id);
 }
 
 cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    const DenseArgs d{p.x, p.w_gate, nullptr, nullptr, s.S, s.d, s.E, 0, 0, p.logit_off, p.ws + L.logits, nullptr,
-                      DENSE_F32, 0};
+    const DenseArgs d{p.x, nullptr, {p.w_gate, nullptr, nullptr}, s.S, s.d, 0, {s.E, 0, 0}, p.logit_off,
+                      {p.ws + L.logits, nullptr, nullptr}, {DENSE_F32, 0, 0}};
     return launch_dense_rn<128>(d, false, reinterpret_cast<StatusBlock*>(p.ws + L.status), st, K_ROUTER);
 }
 

@@ -57,6 +57,10 @@ CASES = [
     mi.LatentConfig("lg_s3_noshared", S=3, H=384, LAT=256, E=16, k=2, I=256, SI=0),
     mi.LatentConfig("lg_s20_zipf", S=20, H=256, LAT=384, E=12, k=3, I=128, SI=256, zipf=1.1),
     mi.LatentConfig("lg_s1", S=1, H=128, LAT=128, E=4, k=1, I=128, SI=128),
+    # E a multiple of 128: the router's rows join the latent-down launch
+    # (with the shared gate/up: three products of x in one launch; without it, two)
+    mi.LatentConfig("lg_s5_router_part", S=5, H=256, LAT=256, E=128, k=4, I=128, SI=256),
+    mi.LatentConfig("lg_s2_router_part_noshared", S=2, H=384, LAT=128, E=256, k=2, I=256, SI=0, zipf=1.1),
 ]
 
 
