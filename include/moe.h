@@ -123,8 +123,10 @@ const char* moe_strerror(int code);
 int moe_workspace_bytes(const moe_shape* shape, size_t* bytes);
 
 /*
- * Clears the workspace's status block (enqueued on `stream`).  Call once after
- * allocating a workspace, before its first use.
+ * Clears the workspace's status block and its per-expert sort counters (the
+ * first 6400 bytes, or ws_bytes if fewer; enqueued on `stream`).  Call once
+ * after allocating a workspace, before its first use; the library's kernels
+ * leave the counters cleared after every call that completes.
  */
 int moe_workspace_init(void* ws, size_t ws_bytes, void* stream);
 

@@ -33,6 +33,7 @@ WsLayout ws_layout(const moe_shape& s) {
     size_t o = 0;
     auto take = [&](size_t bytes) { size_t at = o; o = align256(o + bytes); return at; };
     L.status = take(sizeof(StatusBlock));
+    L.sortcnt = take(SORT_CNT_BYTES);   // right after the status block: the zeroed prefix
     // router K-split (its cluster size): chosen for 152 SMs (GB300); another
     // SM count only changes how the work is split
     L.router_kslices = router_kslices(s, 152);
@@ -215,7 +216,8 @@ int moe_workspace_init(void* ws, size_t ws_bytes, void* stream) {
     if (ws_bytes < sizeof(StatusBlock)) return MOE_ERR_WORKSPACE;
     int rc = check_device();
     if (rc) return rc;
-    return cuda_rc(cudaMemsetAsync(ws, 0, sizeof(StatusBlock), (cudaStream_t)stream));
+    const size_t n = ws_bytes < WS_ZERO_PREFIX ? ws_bytes : WS_ZERO_PREFIX;
+    return cuda_rc(cudaMemsetAsync(ws, 0, n, (cudaStream_t)stream));
 }
 
 int moe_route(const moe_shape* shape, const void* x, const void* w_gate, const float* bias,

@@ -23,7 +23,8 @@ struct StatusBlock {
     int32_t n_tiles;    // gate_up work tiles of the current call
     int32_t work_next;  // persistent-kernel work counters (reset each call)
     int32_t work_next2;
-    int32_t pad[58];
+    int32_t count_done; // CTAs of the counting kernel done (its last CTA resets it)
+    int32_t pad[57];
 };
 static_assert(sizeof(StatusBlock) == 256, "status block is 256 bytes");
 
@@ -41,6 +42,14 @@ int tile_picks(const moe_shape& s);
 // the last tile's copy stays inside the table).
 constexpr int TOKEN_SCALE_ROW = 16;
 
+// The sort counters of the picks above 128 (right after the status block):
+// cnt [E] picks per expert, off [E] segment offsets, cnt2 [E] picks placed
+// per expert; E <= 512.  Zero before a call (moe_workspace_init, and every
+// call leaves them so), with the status block the workspace's zeroed prefix.
+constexpr int SORT_CNT_MAX_E = 512;
+constexpr size_t SORT_CNT_BYTES = 3 * SORT_CNT_MAX_E * sizeof(int32_t);
+constexpr size_t WS_ZERO_PREFIX = sizeof(StatusBlock) + SORT_CNT_BYTES;
+
 // One work tile: expert e, first sorted pick p0, n picks (n <= nt).
 struct Tile {
     int32_t e, p0, n, pad;
@@ -48,7 +57,7 @@ struct Tile {
 
 // Byte offsets of the workspace regions (all 256-byte aligned).
 struct WsLayout {
-    size_t status, logits, pos, tiles, tile_ready, xq, xs, hq, hs, y, ssq;
+    size_t status, sortcnt, logits, pos, tiles, tile_ready, xq, xs, hq, hs, y, ssq;
     size_t xin, hio_ids, hio_w, hio_out;  // moe_forward_host staging
     size_t total;
     int max_tiles;

@@ -84,8 +84,8 @@ extern "C" int moe_forward_noalloc(const moe_shape* shape, const void* x, const 
     if (rc) return rc;
     cudaStream_t st = (cudaStream_t)stream;
     // the array keeps the previous call's contents: the status block (error
-    // latch, per-call counters) must start at zero
-    if (cudaMemsetAsync(ws, 0, sizeof(StatusBlock), st) != cudaSuccess) {
+    // latch, per-call counters) and the sort counters must start at zero
+    if (cudaMemsetAsync(ws, 0, WS_ZERO_PREFIX, st) != cudaSuccess) {
         cudaGetLastError();
         return MOE_ERR_CUDA;
     }

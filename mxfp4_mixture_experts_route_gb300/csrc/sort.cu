@@ -29,147 +29,17 @@ struct SortOut {
     StatusBlock* sb;
 };
 
-// shared-memory ints of sort_picks: per expert a count, a segment offset and a
-// tile offset (E + 1 each)
-__host__ __device__ constexpr int sort_smem_ints(int E) { return 3 * (E + 1); }
-
-// The pairwise-count sort (sort_picks_small) for up to SMALL_SORT_PICKS picks:
-// each thread then compares at most 16 keys for the pick it counts for; above
-// that the atomic-rank sort (sort_picks).  Shared memory of the sort kernel:
-// the chosen sort's ints (the pairwise count also stages the ids there).
+// The pairwise-count sort (sort_picks_small) of up to SMALL_SORT_PICKS picks
+// (each thread then compares at most 16 keys for the pick it counts for), one
+// CTA; more picks go through k_count and k_gather_tok.  Shared memory: 3 P
+// ints (the keys, the tile starts by position, the staged ids).
 constexpr int SMALL_SORT_PICKS = 128;
-__host__ __device__ constexpr int sort_smem_ints_for(int E, int P) {
-    return P <= SMALL_SORT_PICKS ? 3 * P : sort_smem_ints(E);
-}
 
-// Sort of the S * k picks by expert, one CTA of SORT_THREADS threads.
-//   1. every pick p = t*k + j whose id e is in [0, E) and not repeated by an
-//      earlier pick of token t takes a rank within expert e (a shared-memory
-//      atomic); the others get pos[p] = -1 and latch MOE_ERR_BAD_IDS
-//   2. one warp scans the counts over the experts: segment offsets and tile
-//      offsets
-//   3. every thread places its picks (pos[p] = offset[e] + rank)
-//      and writes tile entries (expert e, first pick, picks in the tile)
-// The order of the picks inside a segment is the order the atomics came in:
-// each pick is an independent column of the expert GEMMs, so the results do
-// not depend on it.  ids is in global memory (an earlier kernel's output,
-// read through L2).
-// Output: pos[S*k], tiles[n_tiles] and n_picks / n_tiles;
-// tile_ready[] zeroed.
-__device__ __forceinline__ void sort_picks(const int32_t* ids, int S, int E, int k, const SortOut& o,
-                                           int32_t* smem) {
-    int32_t* cnt = smem;               // [E + 1] counts
-    int32_t* off = cnt + (E + 1);      // [E + 1] segment offsets
-    int32_t* toff = off + (E + 1);     // [E + 1] tile offsets
-    __shared__ int32_t tot_tiles;
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int P = S * k;
-    const int nt = o.nt;
-    StatusBlock* sb = o.sb;
-
-    for (int i = tid; i <= E; i += SORT_THREADS) cnt[i] = 0;
-    for (int i = tid; i < o.max_tiles; i += SORT_THREADS) o.tile_ready[i] = 0u;
-    __syncthreads();
-
-    // 1 ----------------------------------------------------------------------
-    // the lanes of a warp that hold the same expert share one atomic
-    const uint32_t lower = (1u << lane) - 1u;
-    for (int p0 = warp * 32; p0 < P; p0 += SORT_THREADS) {
-        const int p = p0 + lane;
-        int e = -1;
-        bool ok = false;
-        if (p < P) {
-            const int t = p / k, j = p - t * k;
-            e = ld_dep(ids + p);
-            ok = e >= 0 && e < E;
-            for (int q = 0; q < j && ok; ++q) ok = ld_dep(ids + (size_t)t * k + q) != e;
-        }
-        const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
-        const int leader = __ffs(grp) - 1;
-        int base = 0;
-        if (ok && lane == leader) base = atomicAdd(&cnt[e], __popc(grp));
-        base = __shfl_sync(0xffffffffu, base, leader);
-        if (p < P) {
-            if (ok) {
-                o.pos[p] = base + __popc(grp & lower);   // rank within the expert, for now
-            } else {
-                o.pos[p] = -1;
-                latch_status(sb, MOE_ERR_BAD_IDS, p);
-            }
-        }
-    }
-    __syncthreads();
-
-    // 2 ----------------------------------------------------------------------
-    if (warp == 0) {
-        // lane l scans experts [l*per, (l+1)*per); two exclusive scans at once
-        const int per = (E + 31) / 32;
-        const int e0 = lane * per, e1 = min(E, e0 + per);
-        int sp = 0, st = 0;
-        for (int e = e0; e < e1; ++e) {
-            const int n = cnt[e];
-            sp += n;
-            st += (n + nt - 1) / nt;
-        }
-        int ip = sp, it = st;
-#pragma unroll
-        for (int m = 1; m < 32; m <<= 1) {
-            const int a = __shfl_up_sync(0xffffffffu, ip, m);
-            const int b = __shfl_up_sync(0xffffffffu, it, m);
-            if (lane >= m) {
-                ip += a;
-                it += b;
-            }
-        }
-        int rp = ip - sp, rt = it - st;   // exclusive prefixes of this lane's run
-        for (int e = e0; e < e1; ++e) {
-            const int n = cnt[e];
-            off[e] = rp;
-            toff[e] = rt;
-            rp += n;
-            rt += (n + nt - 1) / nt;
-        }
-        if (lane == 31) {
-            off[E] = ip;
-            toff[E] = it;
-            tot_tiles = it;
-            sb->n_picks = ip;
-            sb->n_tiles = it;
-            sb->work_next = 0;
-            sb->work_next2 = 0;
-        }
-    }
-    __syncthreads();
-
-    // 3 ----------------------------------------------------------------------
-    for (int p = warp * 32 + lane; p < P; p += SORT_THREADS) {
-        const int r = o.pos[p];
-        if (r >= 0) {
-            const int q = off[ld_dep(ids + p)] + r;
-            o.pos[p] = q;
-        }
-    }
-    const int n_tiles = tot_tiles;
-    for (int ti = tid; ti < n_tiles; ti += SORT_THREADS) {
-        // expert of tile ti: the last e with toff[e] <= ti (binary search)
-        int lo = 0, hi = E - 1;
-        while (lo < hi) {
-            const int mid = (lo + hi + 1) >> 1;
-            if (toff[mid] <= ti) lo = mid;
-            else hi = mid - 1;
-        }
-        const int i = ti - toff[lo];
-        Tile tl;
-        tl.e = lo;
-        tl.p0 = off[lo] + i * nt;
-        tl.n = min(nt, cnt[lo] - i * nt);
-        tl.pad = 0;
-        o.tiles[ti] = tl;
-    }
-}
-
-// The same outputs for P = S * k <= SMALL_SORT_PICKS picks, by pairwise counting
-// in one CTA (three barriers, no global round trip).  With key_p = (e_p, p)
+// Sort of the S * k <= SMALL_SORT_PICKS picks by expert, by pairwise counting
+// in one CTA (three barriers, no global round trip).  Every pick p = t*k + j
+// whose id is in [0, E) and not repeated by an earlier pick of token t gets a
+// position; the others get pos[p] = -1 and latch MOE_ERR_BAD_IDS.  Output:
+// pos[S*k], tiles[n_tiles] and n_picks / n_tiles; tile_ready[] zeroed.  With key_p = (e_p, p)
 // over the valid picks, a pick's position is r_p = #{q : key_q < key_p} =
 // lt + eqb, where lt = #{q : e_q < e_p} is the start of expert e_p's segment
 // and eqb = #{q < p : e_q = e_p} the pick's index inside it; the segment's
@@ -256,7 +126,7 @@ __device__ __forceinline__ void sort_picks_small(const int32_t* ids, int S, int 
     }
 }
 
-// moe_experts (ids from the caller): ids in global memory.
+// moe_experts (ids from the caller) with up to 128 picks.
 __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* ids, int S, int E, int k,
                                                        SortOut o) {
     extern __shared__ int32_t smem[];
@@ -264,15 +134,11 @@ __global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* ids, int S
     pdl_wait();
     pdl_trigger();   // after the wait: see launch_gather
     KT_MARK(K_SORT, 1);
-    const int P = S * k;
-    if (P <= SMALL_SORT_PICKS) {
-        int32_t* sids = smem + 2 * P;
-        for (int i = threadIdx.x; i < P; i += SORT_THREADS) sids[i] = ld_dep(ids + i);
-        __syncthreads();
-        sort_picks_small(sids, S, E, k, o, smem);
-    } else {
-        sort_picks(ids, S, E, k, o, smem);
-    }
+    const int P = S * k;   // <= SMALL_SORT_PICKS
+    int32_t* sids = smem + 2 * P;
+    for (int i = threadIdx.x; i < P; i += SORT_THREADS) sids[i] = ld_dep(ids + i);
+    __syncthreads();
+    sort_picks_small(sids, S, E, k, o, smem);
     KT_MARK(K_SORT, 2);
 }
 
@@ -453,6 +319,168 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
     KT_MARK(K_ROUTE_GATHER, 2);
 }
 
+// Whether pick j of token t (id e) is valid: e in [0, E) and not an id of the
+// token's earlier picks, which are read all at once (k <= 16), not one
+// round trip after another.
+__device__ __forceinline__ bool pick_valid(const int32_t* ids, int t, int j, int k, int e, int E) {
+    if (e < 0 || e >= E) return false;
+    int prev[16];
+#pragma unroll
+    for (int q = 0; q < 16; ++q) prev[q] = q < j ? ld_dep(ids + (size_t)t * k + q) : -1;
+    bool ok = true;
+#pragma unroll
+    for (int q = 0; q < 16; ++q) ok = ok && prev[q] != e;
+    return ok;
+}
+
+// Sort of more than 128 picks over many CTAs, for the gather below.
+//   k_count: every pick p = t*k + j whose id e is in [0, E) and not repeated
+//   by an earlier pick of token t counts itself into cnt[e] (warp-aggregated
+//   global atomics; the others latch MOE_ERR_BAD_IDS); the last CTA to finish
+//   (a counter in the status block) turns the counts into segment offsets
+//   off[e] and tile offsets (one warp: two exclusive scans), writes every tile entry
+//   (expert e, first position off[e] + i nt, min(nt, cnt[e] - i nt) picks),
+//   the call's counts, clears cnt, the placement counters cnt2 and tile_ready
+//   for the call, and resets its own counter.
+//   k_gather_tok: one CTA a token: its row quantised once, then each valid
+//   pick takes the position off[e] + atomicAdd(cnt2[e], 1) and gets a copy.
+// The order of the picks inside a segment is the order the atomics came in:
+// each pick is an independent column of the expert GEMMs, so the results do
+// not depend on it; tiles and counts do not either.
+constexpr int CNT_THREADS = 1024;
+struct CountOut {
+    int32_t* cnt;
+    int32_t* off;
+    int32_t* cnt2;
+    SortOut o;
+};
+
+__global__ void __launch_bounds__(CNT_THREADS) k_count(const int32_t* ids, int S, int E, int k, CountOut c) {
+    __shared__ int32_t s_cnt[SORT_CNT_MAX_E], s_off[SORT_CNT_MAX_E + 1], s_toff[SORT_CNT_MAX_E + 1];
+    __shared__ int32_t last;
+    KT_MARK(K_SORT, 0);
+    pdl_wait();
+    pdl_trigger();   // the call's first kernel for moe_experts: see launch_gather
+    KT_MARK(K_SORT, 1);
+    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+    const int P = S * k, p = blockIdx.x * CNT_THREADS + tid;
+    const SortOut& o = c.o;
+    int e = -1;
+    bool ok = false;
+    if (p < P) {
+        const int t = p / k, j = p - t * k;
+        e = ld_dep(ids + p);
+        ok = pick_valid(ids, t, j, k, e, E);
+        if (!ok) latch_status(o.sb, MOE_ERR_BAD_IDS, p);
+    }
+    const uint32_t grp = __match_any_sync(0xffffffffu, ok ? e : -1 - lane);
+    if (ok && lane == __ffs(grp) - 1) atomicAdd(&c.cnt[e], __popc(grp));
+    __threadfence();
+    __syncthreads();
+    if (tid == 0) last = atomicAdd(&o.sb->count_done, 1) == (int)gridDim.x - 1;
+    __syncthreads();
+    if (!last) return;
+    __threadfence();
+    const int nt = o.nt;
+    for (int i = tid; i < E; i += CNT_THREADS) {
+        s_cnt[i] = ld_dep(c.cnt + i);
+        c.cnt[i] = 0;    // clear for the next call
+        c.cnt2[i] = 0;   // placement counters of this call
+    }
+    for (int i = tid; i < o.max_tiles; i += CNT_THREADS) o.tile_ready[i] = 0u;
+    __syncthreads();
+    if (warp == 0) {
+        // lane l scans experts [l*per, (l+1)*per); two exclusive scans at once
+        const int per = (E + 31) / 32;
+        const int e0 = lane * per, e1 = min(E, e0 + per);
+        int sp = 0, st = 0;
+        for (int ee = e0; ee < e1; ++ee) {
+            sp += s_cnt[ee];
+            st += (s_cnt[ee] + nt - 1) / nt;
+        }
+        int ip = sp, it = st;
+#pragma unroll
+        for (int m = 1; m < 32; m <<= 1) {
+            const int a = __shfl_up_sync(0xffffffffu, ip, m);
+            const int b = __shfl_up_sync(0xffffffffu, it, m);
+            if (lane >= m) {
+                ip += a;
+                it += b;
+            }
+        }
+        int rp = ip - sp, rt = it - st;
+        for (int ee = e0; ee < e1; ++ee) {
+            s_off[ee] = rp;
+            s_toff[ee] = rt;
+            rp += s_cnt[ee];
+            rt += (s_cnt[ee] + nt - 1) / nt;
+        }
+        if (lane == 31) {
+            o.sb->n_picks = ip;
+            o.sb->n_tiles = it;
+            o.sb->work_next = 0;
+            o.sb->work_next2 = 0;
+            o.sb->count_done = 0;
+        }
+    }
+    __syncthreads();
+    for (int ee = tid; ee < E; ee += CNT_THREADS) {
+        c.off[ee] = s_off[ee];
+        const int n = s_cnt[ee];
+        for (int i = 0; i * nt < n; ++i) {
+            Tile tl;
+            tl.e = ee;
+            tl.p0 = s_off[ee] + i * nt;
+            tl.n = min(nt, n - i * nt);
+            tl.pad = 0;
+            o.tiles[s_toff[ee] + i] = tl;
+        }
+    }
+    KT_MARK(K_SORT, 2);
+}
+
+// grid (S), a thread per 8 elements of a row (see k_count)
+__global__ void __launch_bounds__(1024) k_gather_tok(const __nv_bfloat16* __restrict__ x, const int32_t* ids, int k,
+                                                    int E, int d, int I, int P, CountOut c,
+                                                    uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
+                                                    uint8_t* __restrict__ hs) {
+    __shared__ int32_t r_sh[16];
+    KT_MARK(K_GATHER, 0);
+    pdl_trigger();
+    const int t = blockIdx.x, tid = threadIdx.x;
+    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
+    const int nc = d / 8;
+    QuantChunk q[GATHER_PASSES];
+#pragma unroll
+    for (int i = 0; i < GATHER_PASSES; ++i) {
+        const int cc = i * (int)blockDim.x + tid;
+        if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, cc, cc < nc);   // block-uniform condition
+    }
+    pdl_wait();
+    KT_MARK(K_GATHER, 1);
+    if (tid < k) {
+        const int p = t * k + tid;
+        const int e = ld_dep(ids + p);
+        const bool ok = pick_valid(ids, t, tid, k, e, E);
+        const int r = ok ? ld_dep(c.off + e) + atomicAdd(&c.cnt2[e], 1) : -1;
+        c.o.pos[p] = r;
+        r_sh[tid] = r;
+    }
+    __syncthreads();
+    const size_t tab_rows = (size_t)P + NT_MAX;
+    for (int j = 0; j < k; ++j) {
+        const int r = r_sh[j];
+        if (r < 0) continue;
+#pragma unroll
+        for (int i = 0; i < GATHER_PASSES; ++i) {
+            const int cc = i * (int)blockDim.x + tid;
+            if (cc < nc) store_chunk(q[i], cc, r, d, tab_rows, xq, xs);
+        }
+        pad_scale_rows(r, d, I, tab_rows, xs, hs, tid);
+    }
+    KT_MARK(K_GATHER, 2);
+}
+
 }  // namespace
 
 static SortOut sort_out(const WsLayout& L, char* ws) {
@@ -483,9 +511,35 @@ static cudaError_t launch_gather(const moe_shape& s, const WsLayout& L, const Pt
     return e;
 }
 
+static CountOut count_out(const WsLayout& L, char* ws) {
+    CountOut c;
+    int32_t* base = reinterpret_cast<int32_t*>(ws + L.sortcnt);
+    c.cnt = base;
+    c.off = base + SORT_CNT_MAX_E;
+    c.cnt2 = base + 2 * SORT_CNT_MAX_E;
+    c.o = sort_out(L, ws);
+    return c;
+}
+
 cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     KT_BIND();
-    const size_t smem = (size_t)sort_smem_ints_for(s.E, s.S * s.k) * sizeof(int32_t);
+    const int P = s.S * s.k;
+    if (P > SMALL_SORT_PICKS) {
+        const CountOut c = count_out(L, p.ws);
+        timing_begin(K_SORT, st);
+        cudaError_t e = launch_pdl(k_count, dim3((P + CNT_THREADS - 1) / CNT_THREADS), dim3(CNT_THREADS), 0, st,
+                                   (const int32_t*)p.ids, s.S, s.E, s.k, c);
+        timing_end(st);
+        if (e != cudaSuccess) return e;
+        const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
+        timing_begin(K_GATHER, st);
+        e = launch_pdl(k_gather_tok, dim3(s.S), dim3(threads), 0, st, p.x, (const int32_t*)p.ids, s.k, s.E, s.d, s.I,
+                       L.max_picks, c, reinterpret_cast<uint8_t*>(p.ws + L.xq), reinterpret_cast<uint8_t*>(p.ws + L.xs),
+                       reinterpret_cast<uint8_t*>(p.ws + L.hs));
+        timing_end(st);
+        return e;
+    }
+    const size_t smem = (size_t)3 * P * sizeof(int32_t);
     timing_begin(K_SORT, st);
     cudaError_t e = launch_pdl(k_sort, dim3(1), dim3(SORT_THREADS), smem, st, (const int32_t*)p.ids, s.S, s.E, s.k,
                                sort_out(L, p.ws));

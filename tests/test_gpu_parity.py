@@ -276,6 +276,44 @@ def test_bad_ids_latch_status():
     assert moe.device_status(blk.ws)[0] == moe.MOE_OK      # cleared
 
 
+def test_bad_ids_latch_status_many_picks():
+    """More than 128 picks (the multi-CTA count and the per-token gather):
+    an out-of-range id and a repeated one latch MOE_ERR_BAD_IDS, are left out
+    of the sums, and every valid pick still contributes."""
+    import torch
+    cfg = mi.MoEConfig("bad_many", S=40, d=256, E=8, k=4, I=128)
+    inp = mi.make_inputs(cfg, 4, use_stored_attempts=False)
+    blk = device_block(inp)
+    s = blk.shape
+    rng = np.random.default_rng(11)
+    ids_np = np.stack([np.sort(rng.choice(cfg.E, cfg.k, replace=False)) for _ in range(cfg.S)]).astype(np.int32)
+    w_np = np.full((cfg.S, cfg.k), 0.25, np.float32)
+    ids_np[7, 2] = 8                      # out of range
+    ids_np[30, 3] = ids_np[30, 0]         # repeated within token 30
+    moe.experts(s, blk.x, torch.as_tensor(ids_np).cuda(), torch.as_tensor(w_np).cuda(), blk.w13, blk.w13s, blk.w2,
+                blk.w2s, None, blk.out, blk.ws)
+    rc, det = moe.device_status(blk.ws)
+    assert rc == moe.MOE_ERR_BAD_IDS and det in (7 * 4 + 2, 30 * 4 + 3)
+    out = blk.out.cpu().numpy()
+    xf = O.bf16_to_f64(inp.x)
+    for t in (7, 30, 0):
+        valid = [j for j in range(cfg.k) if 0 <= ids_np[t, j] < cfg.E and ids_np[t, j] not in ids_np[t, :j]]
+        ref = sum(0.25 * O.expert_ffn(xf[t:t + 1], inp.w13[e], inp.w13s[e], inp.w2[e], inp.w2s[e])[0]
+                  for e in ids_np[t, valid])
+        assert O.parity_error(out[t], ref) <= OUT_TOL
+    assert moe.device_status(blk.ws)[0] == moe.MOE_OK      # cleared
+    # the counters are left clear: a valid call on the same workspace matches the oracle
+    good = np.stack([np.sort(rng.choice(cfg.E, cfg.k, replace=False)) for _ in range(cfg.S)]).astype(np.int32)
+    moe.experts(s, blk.x, torch.as_tensor(good).cuda(), torch.as_tensor(w_np).cuda(), blk.w13, blk.w13s, blk.w2,
+                blk.w2s, None, blk.out, blk.ws)
+    moe.check_device_status(blk.ws, "second call")
+    out = blk.out.cpu().numpy()
+    for t in (0, 7, 39):
+        ref = sum(0.25 * O.expert_ffn(xf[t:t + 1], inp.w13[e], inp.w13s[e], inp.w2[e], inp.w2s[e])[0]
+                  for e in good[t])
+        assert O.parity_error(out[t], ref) <= OUT_TOL
+
+
 def test_bad_scale_latches_status():
     # e8m0 255 is NaN (OCP MX v1.0); it is reported, not silently used
     inp = mi.make_inputs(mi.CONFIGS[0])
