@@ -46,7 +46,7 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
                                                        const __nv_bfloat16* __restrict__ wg,
                                                        const float* __restrict__ off, float* __restrict__ L,
                                                        int S, int d, int E, int kslices) {
-    __shared__ uint4 xs_[RT_TOKENS * (RT_KC / 8)];
+    __shared__ uint4 xs_[2][RT_TOKENS * (RT_KC / 8)];
     __shared__ float part[RT_TOKENS * RT_EXPERTS];
     KT_MARK(K_ROUTER, 0);
     const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -58,29 +58,15 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
     float acc[RT_TOKENS];
 #pragma unroll
     for (int t = 0; t < RT_TOKENS; ++t) acc[t] = 0.f;
-    for (int kc = k_begin; kc < k_end; kc += RT_KC) {
-        const int klen = min(RT_KC, k_end - kc);             // 256 or 128
-        const int q16 = klen / 8;                            // 16-byte pieces of a row slice
-        uint4 w = make_uint4(0, 0, 0, 0);
-        if (e < E && lane < q16) w = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)e * d + kc) + lane);
-        if (kc == k_begin) {
-            pdl_wait();      // the first weight slice is in flight; x may come from the stream's last kernel
-            pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
-            KT_MARK(K_ROUTER, 1);
-        }
-        __syncthreads();
-        for (int i = threadIdx.x; i < nt * q16; i += RT_THREADS) {
-            const int r = i / q16, c = i % q16;
-            xs_[r * (RT_KC / 8) + c] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * d + kc) + c);
-        }
-        __syncthreads();
+    // one 256-K round: the lane's 8 weights against every staged token row
+    auto fma_round = [&](const uint4 w, const uint4* xr, int q16) {
         if (lane < q16) {
             const float w0 = bf_lo(w.x), w1 = bf_hi(w.x), w2 = bf_lo(w.y), w3 = bf_hi(w.y);
             const float w4 = bf_lo(w.z), w5 = bf_hi(w.z), w6 = bf_lo(w.w), w7 = bf_hi(w.w);
 #pragma unroll
             for (int t = 0; t < RT_TOKENS; ++t) {
                 if (t < nt) {
-                    const uint4 v = xs_[t * (RT_KC / 8) + lane];
+                    const uint4 v = xr[t * (RT_KC / 8) + lane];
                     float a = acc[t];
                     a = fmaf(bf_lo(v.x), w0, a);
                     a = fmaf(bf_hi(v.x), w1, a);
@@ -93,6 +79,50 @@ __global__ void __launch_bounds__(RT_THREADS) k_router(const __nv_bfloat16* __re
                     acc[t] = a;
                 }
             }
+        }
+    };
+    auto stage = [&](uint4* xr, int kc, int q16) {
+        for (int i = threadIdx.x; i < nt * q16; i += RT_THREADS) {
+            const int r = i / q16, c = i % q16;
+            xr[r * (RT_KC / 8) + c] = __ldg(reinterpret_cast<const uint4*>(x + (size_t)(t0 + r) * d + kc) + c);
+        }
+    };
+    if (k_end - k_begin <= 2 * RT_KC) {
+        // a K range of at most two rounds: both weight slices in flight before
+        // the wait, both rounds of token rows staged at once (one round trip)
+        uint4 w[2];
+        int q16[2];
+#pragma unroll
+        for (int r = 0; r < 2; ++r) {
+            const int kc = k_begin + r * RT_KC;
+            q16[r] = kc < k_end ? min(RT_KC, k_end - kc) / 8 : 0;
+            w[r] = make_uint4(0, 0, 0, 0);
+            if (e < E && lane < q16[r]) w[r] = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)e * d + kc) + lane);
+        }
+        pdl_wait();      // x may come from the stream's last kernel
+        pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
+        KT_MARK(K_ROUTER, 1);
+#pragma unroll
+        for (int r = 0; r < 2; ++r)
+            if (q16[r] > 0) stage(xs_[r], k_begin + r * RT_KC, q16[r]);
+        __syncthreads();
+#pragma unroll
+        for (int r = 0; r < 2; ++r) fma_round(w[r], xs_[r], q16[r]);
+    } else {
+        for (int kc = k_begin; kc < k_end; kc += RT_KC) {
+            const int klen = min(RT_KC, k_end - kc);             // 256 or 128
+            const int q16 = klen / 8;                            // 16-byte pieces of a row slice
+            uint4 w = make_uint4(0, 0, 0, 0);
+            if (e < E && lane < q16) w = __ldg(reinterpret_cast<const uint4*>(wg + (size_t)e * d + kc) + lane);
+            if (kc == k_begin) {
+                pdl_wait();      // the first weight slice is in flight; x may come from the stream's last kernel
+                pdl_trigger();   // the call's first kernel: successors start once the call's inputs are final
+                KT_MARK(K_ROUTER, 1);
+            }
+            __syncthreads();
+            stage(xs_[0], kc, q16);
+            __syncthreads();
+            fma_round(w, xs_[0], q16);
         }
     }
 #pragma unroll
