@@ -118,10 +118,13 @@ __device__ uint64_t g_trace[TR_MAX_CTAS][TR_KINDS][TR_CAP];
 
 #ifndef MOE_WAIT_TEST
 constexpr uint64_t WAIT_NS = 2000000000ull;  // bounded waits: 2 s
+constexpr uint64_t WAIT_NS_H = WAIT_NS;      // the token producer's wait for a tile's h rows
 #else
 // test-only build: waits give up after 1 ms, and one down unit can be made to
-// wait for a readiness count that is never reached
+// wait for a readiness count that is never reached; that wait gives up first
+// (the waits behind it, on the unit's MMAs, would run out 1 ms after they began)
 constexpr uint64_t WAIT_NS = 1000000ull;
+constexpr uint64_t WAIT_NS_H = WAIT_NS / 4;
 int g_unreachable_wait = 0;
 #endif
 
@@ -600,7 +603,7 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                     const uint32_t target = h_target(U);
                     while (!U.h_ready && ptx::ld_acquire_gpu(&a.tile_ready[U.tile]) < target) {
                         __nanosleep(32);
-                        if ((++it & 63u) == 0u && (*abort_flag || ptx::globaltimer() - t0 > WAIT_NS)) {
+                        if ((++it & 63u) == 0u && (*abort_flag || ptx::globaltimer() - t0 > WAIT_NS_H)) {
                             fail(2);
                             ready = 0;
                             break;
