@@ -18,8 +18,6 @@ namespace moe {
 
 namespace {
 
-constexpr int SORT_THREADS = 1024;
-
 struct SortOut {
     int32_t* pos;
     Tile* tiles;
@@ -29,169 +27,28 @@ struct SortOut {
     StatusBlock* sb;
 };
 
-// The pairwise-count sort (sort_picks_small) of up to SMALL_SORT_PICKS picks
-// (each thread then compares at most 16 keys for the pick it counts for), one
-// CTA; more picks go through k_count and k_gather_tok.  Shared memory: 3 P
-// ints (the keys, the tile starts by position, the staged ids).
-constexpr int SMALL_SORT_PICKS = 128;
-
-// Sort of the S * k <= SMALL_SORT_PICKS picks by expert, by pairwise counting
-// in one CTA (three barriers, no global round trip).  Every pick p = t*k + j
-// whose id is in [0, E) and not repeated by an earlier pick of token t gets a
-// position; the others get pos[p] = -1 and latch MOE_ERR_BAD_IDS.  Output:
-// pos[S*k], tiles[n_tiles] and n_picks / n_tiles; tile_ready[] zeroed.  With key_p = (e_p, p)
-// over the valid picks, a pick's position is r_p = #{q : key_q < key_p} =
-// lt + eqb, where lt = #{q : e_q < e_p} is the start of expert e_p's segment
-// and eqb = #{q < p : e_q = e_p} the pick's index inside it; the segment's
-// length is eqt = #{q : e_q = e_p}.  Tile starts are the positions with
-// eqb mod nt = 0, numbered in position order by a ballot scan.  Inside a
-// segment the picks keep their order p.  ids is in shared memory; smem holds
-// 2 P ints.
-__device__ __forceinline__ void sort_picks_small(const int32_t* ids, int S, int E, int k, const SortOut& o,
-                                                 int32_t* smem) {
-    constexpr int NONE = 0x7fffffff;
-    int32_t* key = smem;            // [P] expert of pick p, NONE if the pick is not valid
-    int32_t* start = key + S * k;   // [P] by position: (expert << 8 | picks) of the tile starting there, or -1
-    __shared__ int32_t wcnt[SORT_THREADS / 32];
-    const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-    const int P = S * k, nt = o.nt;
-    StatusBlock* sb = o.sb;
-
-    for (int i = tid; i < o.max_tiles; i += SORT_THREADS) o.tile_ready[i] = 0u;
-    int valid = 0;
-    if (tid < P) {
-        const int t = tid / k, j = tid - t * k;
-        const int e = ids[tid];
-        valid = e >= 0 && e < E;
-        for (int q = 0; q < j && valid; ++q) valid = ids[t * k + q] != e;
-        key[tid] = valid ? e : NONE;
-        start[tid] = -1;
-        if (!valid) {
-            o.pos[tid] = -1;
-            latch_status(sb, MOE_ERR_BAD_IDS, tid);
-        }
-    }
-    const int n_valid = __syncthreads_count(valid);
-
-    // G threads (a power of two, at most a warp) count for one pick
-    int G = 32;
-    while (G > 1 && G * P > SORT_THREADS) G >>= 1;
-    const int p = tid / G, c = tid & (G - 1);
-    const int ep = p < P ? key[p] : NONE;
-    int lt = 0, eqb = 0, eqt = 0;
-    if (ep != NONE) {
-        for (int q = c; q < P; q += G) {
-            const int eq = key[q];
-            lt += eq < ep ? 1 : 0;
-            eqt += eq == ep ? 1 : 0;
-            eqb += (eq == ep && q < p) ? 1 : 0;
-        }
-    }
-    for (int m = 1; m < G; m <<= 1) {
-        lt += __shfl_xor_sync(0xffffffffu, lt, m);
-        eqt += __shfl_xor_sync(0xffffffffu, eqt, m);
-        eqb += __shfl_xor_sync(0xffffffffu, eqb, m);
-    }
-    if (c == 0 && ep != NONE) {
-        const int r = lt + eqb;
-        o.pos[p] = r;
-        if (eqb % nt == 0) start[r] = ep << 8 | min(nt, eqt - eqb);
-    }
-    __syncthreads();
-
-    // tile numbers: tile starts counted in position order
-    const int st = tid < n_valid ? start[tid] : -1;
-    const uint32_t bal = __ballot_sync(0xffffffffu, st >= 0);
-    if (lane == 0) wcnt[warp] = __popc(bal);
-    __syncthreads();
-    int before = 0, total = 0;
-    for (int w = 0; w < SORT_THREADS / 32; ++w) {
-        const int n = wcnt[w];
-        before += w < warp ? n : 0;
-        total += n;
-    }
-    if (st >= 0) {
-        Tile tl;
-        tl.e = st >> 8;
-        tl.p0 = tid;
-        tl.n = st & 255;
-        tl.pad = 0;
-        o.tiles[before + __popc(bal & ((1u << lane) - 1u))] = tl;
-    }
-    if (tid == 0) {
-        sb->n_picks = n_valid;
-        sb->n_tiles = total;
-        sb->work_next = 0;
-        sb->work_next2 = 0;
-    }
-}
-
-// moe_experts (ids from the caller) with up to 128 picks.
-__global__ void __launch_bounds__(SORT_THREADS) k_sort(const int32_t* ids, int S, int E, int k,
-                                                       SortOut o) {
-    extern __shared__ int32_t smem[];
-    KT_MARK(K_SORT, 0);
-    pdl_wait();
-    pdl_trigger();   // after the wait: see launch_gather
-    KT_MARK(K_SORT, 1);
-    const int P = S * k;   // <= SMALL_SORT_PICKS
-    int32_t* sids = smem + 2 * P;
-    for (int i = threadIdx.x; i < P; i += SORT_THREADS) sids[i] = ld_dep(ids + i);
-    __syncthreads();
-    sort_picks_small(sids, S, E, k, o, smem);
-    KT_MARK(K_SORT, 2);
-}
-
-// Token rows of the expert GEMMs.  grid (S * k), one pick p = t * k + j a
-// CTA, blockDim = d / 8 rounded up to a warp (at most 1024): the CTA
-// quantises token t's row (quantize_chunk) before it waits for the sort --
-// x is an input of the call, final before the call's first kernel lets its
-// successors start -- and then writes it to the pick's sorted position.
-constexpr int GATHER_PASSES = 2;   // d <= 16384
-__global__ void __launch_bounds__(1024) k_quant_gather(const __nv_bfloat16* __restrict__ x,
-                                                      const int32_t* pos, int k, int d, int I, int P,
-                                                      uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
-                                                      uint8_t* __restrict__ hs) {
-    KT_MARK(K_GATHER, 0);
-    pdl_trigger();
-    const int p = blockIdx.x, t = p / k;
-    const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
-    const int nc = d / 8;
-    QuantChunk q[GATHER_PASSES];
-#pragma unroll
-    for (int i = 0; i < GATHER_PASSES; ++i) {
-        const int c = i * (int)blockDim.x + (int)threadIdx.x;
-        if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, c, c < nc);   // block-uniform condition
-    }
-    KT_MARK(K_GATHER, 3);
-    pdl_wait();
-    KT_MARK(K_GATHER, 1);
-    const int r = ld_dep(pos + p);
-    if (r < 0) return;   // not a valid pick
-    const size_t tab_rows = (size_t)P + NT_MAX;
-#pragma unroll
-    for (int i = 0; i < GATHER_PASSES; ++i) {
-        const int c = i * (int)blockDim.x + (int)threadIdx.x;
-        if (c < nc) store_chunk(q[i], c, r, d, tab_rows, xq, xs);
-    }
-    pad_scale_rows(r, d, I, tab_rows, xs, hs, threadIdx.x);
-    KT_MARK(K_GATHER, 2);
-}
+constexpr int GATHER_PASSES = 2;   // chunks of 8 elements a thread of k_gather_tok: d <= 16384
+constexpr int SMALL_SORT_PICKS = 128;   // up to this many picks, moe_experts places them in k_route_gather
 
 // moe_forward at small S: the top k of every token, the sort of all S * k
 // picks and the gather in one kernel.  grid (S * k), one pick p = t * k + j a
 // CTA, as the gather.  Every CTA selects every token's top k (a warp takes
 // one or two tokens, topk_select) into shared memory, from the same logits
 // with the same code, so all CTAs hold the same ids.  Each then places only
-// its own pick, as sort_picks_small would: with cnt[e] the picks of expert e,
+// its own pick, in the order of a stable sort by expert: with cnt[e] the picks of expert e,
 // r_p = sum_{e < e_p} cnt[e] + #{q < p : e_q = e_p}; a tile opens where that
 // index inside the segment is a multiple of nt, and tiles are numbered in
 // position order: sum_{e < e_p} ceil(cnt[e] / nt) + index / nt.  It writes
 // ids[p], weights[p], pos[p], that tile entry when its pick opens one, and
 // token t's row (quantised before the wait) at r_p; CTA 0 writes the counts.
 // The picks of a token are distinct valid experts.  With FROM_IDS the ids
-// come from the top-k kernel instead (more tokens than each CTA should select
-// again): every CTA reads them and only places and gathers.  The rows are
+// come from the top-k kernel (more tokens than each CTA should select again)
+// or from moe_experts' caller (up to 128 picks): every CTA reads them, checks
+// them (an id out of range or repeated by an earlier pick of its token is left
+// out, latching MOE_ERR_BAD_IDS), and only places and gathers.  As the first
+// kernel of moe_experts it reads x before its wait like every gather: the
+// caller's kernel that wrote x has completed before it may start, and none of
+// the library's kernels writes x.  The rows are
 // quantised before the wait when they are an input of the call, after it
 // when an earlier kernel of the call wrote them (x_after_wait).
 constexpr int RG_THREADS = 512;        // at most; 16 warps: two tokens a warp at S = 32
@@ -210,9 +67,10 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
     pdl_trigger();
     const int P = S * k, nt = o.nt;
     __shared__ int32_t r_sh;
-    int32_t* key = smem;           // [P] expert of pick q = t * k + j
+    int32_t* key = smem;           // [P] expert of pick q = t * k + j (-1: not a valid pick)
     int32_t* cnt = key + P;        // [E] picks of expert e
-    float* s_sh = reinterpret_cast<float*>(cnt + E);   // [min(S, warps)][32 * MAXE]
+    float* s_sh = reinterpret_cast<float*>(cnt + E);   // [min(S, warps)][32 * MAXE] (selecting)
+    int32_t* raw = cnt + E;        // [P] the ids as given (FROM_IDS)
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5, nw = (int)blockDim.x >> 5;
     const int p = blockIdx.x, t = p / k;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
@@ -238,7 +96,18 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
         }
     }
     if constexpr (FROM_IDS) {
-        for (int i = tid; i < P; i += blockDim.x) key[i] = ld_dep(ids + i);
+        // ids from the top-k kernel or from the caller: a pick is valid when its
+        // id is in [0, E) and not an id of an earlier pick of its token; the
+        // others are left out (pos = -1) and latch MOE_ERR_BAD_IDS
+        for (int i = tid; i < P; i += blockDim.x) raw[i] = ld_dep(ids + i);
+        __syncthreads();
+        for (int i = tid; i < P; i += blockDim.x) {
+            const int t2 = i / k, j = i - t2 * k, e = raw[i];
+            bool ok = e >= 0 && e < E;
+            for (int q2 = 0; q2 < j && ok; ++q2) ok = raw[t2 * k + q2] != e;
+            key[i] = ok ? e : -1;
+            if (!ok && p == 0) latch_status(o.sb, MOE_ERR_BAD_IDS, i);
+        }
     } else {
         // the warp's tokens warp and warp + nw: both rows of logits in flight first
         float z[RG_TOKENS_PER_WARP][MAXE];
@@ -264,11 +133,12 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
     }
     __syncthreads();
     KT_MARK(K_ROUTE_GATHER, 3);
-    for (int i = tid; i < P; i += blockDim.x) atomicAdd(&cnt[key[i]], 1);
+    for (int i = tid; i < P; i += blockDim.x)
+        if (key[i] >= 0) atomicAdd(&cnt[key[i]], 1);
     __syncthreads();
     if (warp == 0) {
         const int ep = key[p];
-        int off = 0, toff = 0, ntiles = 0;
+        int off = 0, toff = 0, ntiles = 0, nvalid = 0;
         for (int e0 = 0; e0 < E; e0 += 32) {
             const int e = e0 + lane;
             const int n = e < E ? cnt[e] : 0;
@@ -276,20 +146,22 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
             off += e < ep ? n : 0;
             toff += e < ep ? tn : 0;
             ntiles += tn;
+            nvalid += n;
         }
         off = __reduce_add_sync(0xffffffffu, off);
         toff = __reduce_add_sync(0xffffffffu, toff);
         ntiles = __reduce_add_sync(0xffffffffu, ntiles);
+        nvalid = __reduce_add_sync(0xffffffffu, nvalid);
         int idx = 0;   // picks of expert ep before p
         for (int q0 = 0; q0 < p; q0 += 32) {
             const int qq = q0 + lane;
             idx += __popc(__ballot_sync(0xffffffffu, qq < p && key[qq] == ep));
         }
         if (lane == 0) {
-            const int r = off + idx;
+            const int r = ep >= 0 ? off + idx : -1;
             r_sh = r;
             o.pos[p] = r;
-            if (idx % nt == 0) {
+            if (ep >= 0 && idx % nt == 0) {
                 Tile tl;
                 tl.e = ep;
                 tl.p0 = r;
@@ -298,7 +170,7 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
                 o.tiles[toff + idx / nt] = tl;
             }
             if (p == 0) {
-                o.sb->n_picks = P;
+                o.sb->n_picks = nvalid;
                 o.sb->n_tiles = ntiles;
                 o.sb->work_next = 0;
                 o.sb->work_next2 = 0;
@@ -310,12 +182,14 @@ __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, con
     const int r = r_sh;
     for (int i = p + (int)gridDim.x * tid; i < o.max_tiles; i += (int)gridDim.x * (int)blockDim.x) o.tile_ready[i] = 0u;
     const size_t tab_rows = (size_t)P_tab + NT_MAX;
+    if (r >= 0) {
 #pragma unroll
-    for (int i = 0; i < PASSES; ++i) {
-        const int cc = i * (int)blockDim.x + tid;
-        if (cc < nc) store_chunk(q[i], cc, r, d, tab_rows, xq, xs);
+        for (int i = 0; i < PASSES; ++i) {
+            const int cc = i * (int)blockDim.x + tid;
+            if (cc < nc) store_chunk(q[i], cc, r, d, tab_rows, xq, xs);
+        }
+        pad_scale_rows(r, d, I, tab_rows, xs, hs, tid);
     }
-    pad_scale_rows(r, d, I, tab_rows, xs, hs, tid);
     KT_MARK(K_ROUTE_GATHER, 2);
 }
 
@@ -360,7 +234,7 @@ __global__ void __launch_bounds__(CNT_THREADS) k_count(const int32_t* ids, int S
     __shared__ int32_t last;
     KT_MARK(K_SORT, 0);
     pdl_wait();
-    pdl_trigger();   // the call's first kernel for moe_experts: see launch_gather
+    pdl_trigger();   // the call's first kernel for moe_experts: k_gather_tok reads x before its wait
     KT_MARK(K_SORT, 1);
     const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
     const int P = S * k, p = blockIdx.x * CNT_THREADS + tid;
@@ -494,23 +368,6 @@ static SortOut sort_out(const WsLayout& L, char* ws) {
     return o;
 }
 
-// The gather reads x before its wait.  That is safe because the first kernel
-// of every call (the router, or the sort for moe_experts) lets its successors
-// start only after its own wait has returned, i.e. after the stream's work
-// before the call -- which wrote x -- has completed.
-static cudaError_t launch_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    char* ws = p.ws;
-    KT_BIND();
-    timing_begin(K_GATHER, st);
-    const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
-    const cudaError_t e = launch_pdl(k_quant_gather, dim3(s.S * s.k), dim3(threads), 0, st, p.x,
-                                     reinterpret_cast<const int32_t*>(ws + L.pos), s.k, s.d, s.I, L.max_picks,
-                                     reinterpret_cast<uint8_t*>(ws + L.xq), reinterpret_cast<uint8_t*>(ws + L.xs),
-                                     reinterpret_cast<uint8_t*>(ws + L.hs));
-    timing_end(st);
-    return e;
-}
-
 static CountOut count_out(const WsLayout& L, char* ws) {
     CountOut c;
     int32_t* base = reinterpret_cast<int32_t*>(ws + L.sortcnt);
@@ -521,32 +378,6 @@ static CountOut count_out(const WsLayout& L, char* ws) {
     return c;
 }
 
-cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    KT_BIND();
-    const int P = s.S * s.k;
-    if (P > SMALL_SORT_PICKS) {
-        const CountOut c = count_out(L, p.ws);
-        timing_begin(K_SORT, st);
-        cudaError_t e = launch_pdl(k_count, dim3((P + CNT_THREADS - 1) / CNT_THREADS), dim3(CNT_THREADS), 0, st,
-                                   (const int32_t*)p.ids, s.S, s.E, s.k, c);
-        timing_end(st);
-        if (e != cudaSuccess) return e;
-        const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
-        timing_begin(K_GATHER, st);
-        e = launch_pdl(k_gather_tok, dim3(s.S), dim3(threads), 0, st, p.x, (const int32_t*)p.ids, s.k, s.E, s.d, s.I,
-                       L.max_picks, c, reinterpret_cast<uint8_t*>(p.ws + L.xq), reinterpret_cast<uint8_t*>(p.ws + L.xs),
-                       reinterpret_cast<uint8_t*>(p.ws + L.hs));
-        timing_end(st);
-        return e;
-    }
-    const size_t smem = (size_t)3 * P * sizeof(int32_t);
-    timing_begin(K_SORT, st);
-    cudaError_t e = launch_pdl(k_sort, dim3(1), dim3(SORT_THREADS), smem, st, (const int32_t*)p.ids, s.S, s.E, s.k,
-                               sort_out(L, p.ws));
-    timing_end(st);
-    if (e != cudaSuccess) return e;
-    return launch_gather(s, L, p, st);
-}
 
 // The fused top-k + sort + gather selects again in every CTA; above this
 // many picks (as many CTAs) the top-k kernel selects once and the fused
@@ -575,7 +406,8 @@ static cudaError_t launch_rg(const moe_shape& s, const WsLayout& L, const Ptrs& 
     const int threads = route_gather_threads(s);
     const int P = s.S * s.k;
     const size_t smem = (size_t)(P + s.E) * sizeof(int32_t) +
-                        (FROM_IDS ? 0 : (size_t)std::min(s.S, threads / 32) * 32 * MAXE * sizeof(float));
+                        (FROM_IDS ? (size_t)P * sizeof(int32_t)
+                                  : (size_t)std::min(s.S, threads / 32) * 32 * MAXE * sizeof(float));
     const int passes = (s.d / 8 + threads - 1) / threads;   // 1, 2 or 4 (d <= 16384)
     auto kern = passes == 1 ? k_route_gather<MAXE, 1, FROM_IDS>
                             : passes == 2 ? k_route_gather<MAXE, 2, FROM_IDS> : k_route_gather<MAXE, 4, FROM_IDS>;
@@ -600,6 +432,29 @@ cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const
         return launch_rg<8, true>(s, L, p, st, x_after_wait);
     }
     return s.E <= 256 ? launch_rg<8, false>(s, L, p, st, x_after_wait) : launch_rg<16, false>(s, L, p, st, x_after_wait);
+}
+
+cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    KT_BIND();
+    const int P = s.S * s.k;
+    if (P > SMALL_SORT_PICKS) {
+        const CountOut c = count_out(L, p.ws);
+        timing_begin(K_SORT, st);
+        cudaError_t e = launch_pdl(k_count, dim3((P + CNT_THREADS - 1) / CNT_THREADS), dim3(CNT_THREADS), 0, st,
+                                   (const int32_t*)p.ids, s.S, s.E, s.k, c);
+        timing_end(st);
+        if (e != cudaSuccess) return e;
+        const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
+        timing_begin(K_GATHER, st);
+        e = launch_pdl(k_gather_tok, dim3(s.S), dim3(threads), 0, st, p.x, (const int32_t*)p.ids, s.k, s.E, s.d, s.I,
+                       L.max_picks, c, reinterpret_cast<uint8_t*>(p.ws + L.xq), reinterpret_cast<uint8_t*>(p.ws + L.xs),
+                       reinterpret_cast<uint8_t*>(p.ws + L.hs));
+        timing_end(st);
+        return e;
+    }
+    // up to 128 picks: the fused kernel reads the ids, checks them, places
+    // every pick and gathers its row in one launch
+    return launch_rg<8, true>(s, L, p, st, false);
 }
 
 }  // namespace moe
