@@ -3,9 +3,12 @@
 
 A step is one whole forward of the block (router, top-k, expert sort and
 gather, gate_up, down, combine) over one batch of S token rows with all
-weights resident in HBM.  The L2 is flushed (a write of twice its size)
-before every step, outside the timed events; each step is bracketed by CUDA
-events on the launch stream.  Under torchrun each rank runs an independent
+weights resident in HBM.  The L2 is flushed before every step, outside the
+timed events: a write of twice its size, then a read of another buffer of
+twice its size, so that L2 holds none of the step's data and none of the
+flush's dirty lines (whose write-back would otherwise land inside the step:
+2 us at S = 8, 35 us at S = 128; the line also reports the step after the
+write alone).  Each step is bracketed by CUDA events on the launch stream.  Under torchrun each rank runs an independent
 replica (the block does not shard on one box); value = all ranks' tokens / the
 slowest rank's time.
 
@@ -285,7 +288,8 @@ def run_reference(args, cfg: mi.MoEConfig):
 def workload_config(cfg: mi.MoEConfig, n_touched):
     c = {"workload": cfg.name, "S": cfg.S, "d": cfg.d, "E": cfg.E, "k": cfg.k, "I": cfg.I,
          "post_norm": cfg.post_norm, "zipf": cfg.zipf, "seed": 0,
-         "l2": "flushed before every timed step (write of 2x the L2 size, outside the events)"}
+         "l2": "flushed before every timed step, outside the events: a write of 2x the L2 size, "
+               "then a read of another 2x-L2 buffer (L2 left clean)"}
     if n_touched is not None:
         c["n_touched"] = n_touched
     return c
@@ -294,6 +298,25 @@ def workload_config(cfg: mi.MoEConfig, n_touched):
 # ---------------------------------------------------------------------------
 # our arm
 # ---------------------------------------------------------------------------
+class L2Flush:
+    """The flush before every timed step: a write of 2x the L2 size, then a
+    read of another 2x-L2 buffer, which evicts the written lines (their
+    write-back happens here, not in the step) and leaves only clean lines
+    that no step reads.  write_only=True: the write alone."""
+
+    def __init__(self, dev, l2: int, write_only: bool = False):
+        import torch
+        self.w = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+        self.r = None if write_only else torch.ones(2 * l2 // 4, dtype=torch.float32, device=dev)
+        self.sink = torch.empty((), dtype=torch.float32, device=dev)
+
+    def zero_(self):
+        import torch
+        self.w.zero_()
+        if self.r is not None:
+            torch.sum(self.r, dim=0, out=self.sink)
+
+
 def timed_steps(fn, n, flush, stream, warmup=0):
     """Per-step device milliseconds of fn() over n steps (CUDA events on the
     launch stream), the L2 flushed before every step outside the events."""
@@ -449,7 +472,7 @@ def run_ours(args, cfg: mi.MoEConfig):
     blk = upload(moe, cfg, inp, dev)
     shape = blk.shape
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2, dtype=torch.uint8, device=dev)
+    flush = L2Flush(dev, l2)
     stream = torch.cuda.current_stream(dev)
 
     for _ in range(args.warmup):
@@ -527,6 +550,13 @@ def run_ours(args, cfg: mi.MoEConfig):
                    "api": "moe_experts (sort, gather, expert GEMMs, combine; ids and "
                           "weights from the route, device buffers)"}
 
+    # --- the same step after the write-only flush (L2 left dirty) -------------
+    wo_ms = timed_steps(blk.forward, min(K, 300), L2Flush(dev, l2, write_only=True), stream,
+                        warmup=max(3, args.warmup))
+    write_only = {"ms_per_step": statistics.fmean(wo_ms), "ms_per_step_median": statistics.median(wo_ms),
+                  "value": cfg.S / (statistics.fmean(wo_ms) * 1e-3), "unit": "tokens/s", "steps": len(wo_ms),
+                  "l2": "a write of 2x the L2 size alone: its dirty lines are written back inside the step"}
+
     # --- the other workloads (rank 0 of a replica run only) -------------------
     per_config = None
     if rank == 0 and not args.no_per_config:
@@ -568,6 +598,7 @@ def run_ours(args, cfg: mi.MoEConfig):
             "cpu_baseline": cpu,
             "e2e": e2e,
             "moe_experts": experts_api,
+            "write_only_flush": write_only,
             "per_config": per_config,
             "gpu_launches": launches_per_step * K,
             "launches_per_step": launches_per_step,
