@@ -313,33 +313,43 @@ __global__ void __launch_bounds__(CNT_THREADS) k_count(const int32_t* ids, int S
     KT_MARK(K_SORT, 2);
 }
 
-// grid (S), a thread per 8 elements of a row (see k_count)
+// grid (S), a thread per GATHER_PASSES chunks of 8 elements of a row (see
+// k_count).  The row's loads go out before the wait and are quantised only
+// after the placement (the token's ids read once, each pick's position an
+// L2 round trip), so that the two latencies overlap.
 __global__ void __launch_bounds__(1024) k_gather_tok(const __nv_bfloat16* __restrict__ x, const int32_t* ids, int k,
                                                     int E, int d, int I, int P, CountOut c,
                                                     uint8_t* __restrict__ xq, uint8_t* __restrict__ xs,
                                                     uint8_t* __restrict__ hs) {
-    __shared__ int32_t r_sh[16];
+    __shared__ int32_t r_sh[16], id_sh[16];
     KT_MARK(K_GATHER, 0);
     pdl_trigger();
     const int t = blockIdx.x, tid = threadIdx.x;
     const uint4* in = reinterpret_cast<const uint4*>(x + (size_t)t * d);
     const int nc = d / 8;
-    QuantChunk q[GATHER_PASSES];
+    uint4 raw[GATHER_PASSES];
 #pragma unroll
     for (int i = 0; i < GATHER_PASSES; ++i) {
         const int cc = i * (int)blockDim.x + tid;
-        if (i * (int)blockDim.x < nc) q[i] = quantize_chunk(in, cc, cc < nc);   // block-uniform condition
+        raw[i] = cc < nc ? __ldg(in + cc) : make_uint4(0, 0, 0, 0);
     }
     pdl_wait();
     KT_MARK(K_GATHER, 1);
+    if (tid < k) id_sh[tid] = ld_dep(ids + (size_t)t * k + tid);
+    __syncthreads();
     if (tid < k) {
-        const int p = t * k + tid;
-        const int e = ld_dep(ids + p);
-        const bool ok = pick_valid(ids, t, tid, k, e, E);
+        // a pick is placed when its id is in [0, E) and not an id of an
+        // earlier pick of the token (k_count latched the others)
+        const int e = id_sh[tid];
+        bool ok = e >= 0 && e < E;
+        for (int q2 = 0; q2 < tid; ++q2) ok = ok && id_sh[q2] != e;
         const int r = ok ? ld_dep(c.off + e) + atomicAdd(&c.cnt2[e], 1) : -1;
-        c.o.pos[p] = r;
+        c.o.pos[(size_t)t * k + tid] = r;
         r_sh[tid] = r;
     }
+    QuantChunk q[GATHER_PASSES];
+#pragma unroll
+    for (int i = 0; i < GATHER_PASSES; ++i) q[i] = quantize_vals(raw[i]);
     __syncthreads();
     const size_t tab_rows = (size_t)P + NT_MAX;
     for (int j = 0; j < k; ++j) {
@@ -444,7 +454,8 @@ cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs
                                    (const int32_t*)p.ids, s.S, s.E, s.k, c);
         timing_end(st);
         if (e != cudaSuccess) return e;
-        const int threads = std::min(1024, (s.d / 8 + 31) / 32 * 32);
+        // GATHER_PASSES chunks a thread: several tokens' CTAs an SM
+        const int threads = std::min(1024, ((s.d / 8 + GATHER_PASSES - 1) / GATHER_PASSES + 31) / 32 * 32);
         timing_begin(K_GATHER, st);
         e = launch_pdl(k_gather_tok, dim3(s.S), dim3(threads), 0, st, p.x, (const int32_t*)p.ids, s.k, s.E, s.d, s.I,
                        L.max_picks, c, reinterpret_cast<uint8_t*>(p.ws + L.xq), reinterpret_cast<uint8_t*>(p.ws + L.xs),
