@@ -191,7 +191,7 @@ struct Ptrs {
 };
 
 cudaError_t launch_router_logits(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
-// the router's tensor-core kernel (S >= 64, E a multiple of 128)
+// the router's tensor-core kernel (9 <= S <= 32 or S >= 64, E a multiple of 128)
 bool router_tc_fits(const moe_shape& s);
 cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 // dense bf16 product out[S, N] = x[S, K] . w[N, K]^T on the tensor cores

@@ -1,5 +1,5 @@
 // Dense bf16 products on the tensor cores: the router's logits for batches of
-// 64 tokens and more, and the latent-MoE layer's dense projections (latent
+// 9 to 32 and of 64 tokens and more, and the latent-MoE layer's dense projections (latent
 // down and up, the shared expert), at any batch.
 //
 // vllm.models.muse_spark.amd.mono.kernels.k3, stage A (the router's logits in
@@ -308,7 +308,15 @@ cudaError_t launch_dense_args(const DenseArgs& d, StatusBlock* sb, cudaStream_t 
 
 }  // namespace
 
-bool router_tc_fits(const moe_shape& s) { return s.S >= 64 && s.E % RM == 0 && s.d % RK == 0; }
+// Which batches the router runs on the tensor cores (E a multiple of 128):
+// 9 to 32 tokens in 16-token tiles (S = 32: 10.7 us against 14.5 us for the
+// CUDA-core router), 64 and more in 128-token tiles.  Up to 8 tokens the
+// CUDA-core kernel without staging is faster (the step 53 us against 59 us);
+// at 128 tokens 16-token tiles were slower than 128-token ones (20.8 against
+// 16.7 us: eight token tiles each read all the weights).
+bool router_tc_fits(const moe_shape& s) {
+    return ((s.S >= 9 && s.S <= 32) || s.S >= 64) && s.E % RM == 0 && s.d % RK == 0;
+}
 
 bool dense_fits(int S, int K, int N) { return S >= 1 && N % RM == 0 && K % RK == 0 && K / RK >= 1; }
 
@@ -341,7 +349,11 @@ cudaError_t launch_dense_kcat(const void* x, const void* w, int K, const void* x
 cudaError_t launch_router_tc(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     const DenseArgs d{p.x, nullptr, {p.w_gate, nullptr, nullptr}, s.S, s.d, 0, {s.E, 0, 0}, p.logit_off,
                       {p.ws + L.logits, nullptr, nullptr}, {DENSE_F32, 0, 0}};
-    return launch_dense_rn<128>(d, false, reinterpret_cast<StatusBlock*>(p.ws + L.status), st, K_ROUTER);
+    StatusBlock* sb = reinterpret_cast<StatusBlock*>(p.ws + L.status);
+    // up to 32 tokens, tiles of 16: E/128 x S/16 tiles, K split over a
+    // cluster, spread the weight rows over more CTAs than one 128-token tile
+    if (s.S <= 32) return launch_dense_rn<16>(d, s.S <= 16, sb, st, K_ROUTER);
+    return launch_dense_rn<128>(d, false, sb, st, K_ROUTER);
 }
 
 }  // namespace moe

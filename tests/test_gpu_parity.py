@@ -197,6 +197,12 @@ SMALL = [
     mi.MoEConfig("maxEk", S=4, d=256, E=512, k=16, I=128),  # E and k at their maxima
     mi.MoEConfig("maxd", S=2, d=16384, E=8, k=2, I=128),    # d at its maximum (two gather passes)
     mi.MoEConfig("maxI", S=2, d=256, E=4, k=1, I=8192),     # I at its maximum
+    # E a multiple of 128 above 8 tokens: the router on the tensor cores, in
+    # 16-token tiles up to 32 tokens (one ragged tile; two, the last ragged),
+    # in one ragged 128-token tile at 100
+    mi.MoEConfig("tc9", S=9, d=384, E=128, k=4, I=128),
+    mi.MoEConfig("tc30", S=30, d=256, E=256, k=8, I=128, zipf=1.1),
+    mi.MoEConfig("tc100", S=100, d=512, E=256, k=8, I=128, zipf=1.1),
 ]
 
 
