@@ -940,12 +940,13 @@ __global__ void __launch_bounds__(NUM_THREADS, 1)
                 }
             }
             if (!U.down) {
+                // the writers' h rows, generic stores, are read by other CTAs'
+                // TMA copies: each writer fences its stores against the async
+                // proxy, the barrier orders them before the release (a release
+                // is cumulative over what its thread has synchronised with)
                 if (r < 64) ptx::fence_proxy_async_global();
                 ptx::named_bar_sync(1, 128);
-                if (warp == EPI_WARP0 && lane == 0) {
-                    __threadfence();
-                    ptx::red_release_gpu_add(&a.tile_ready[U.tile], 1u);
-                }
+                if (warp == EPI_WARP0 && lane == 0) ptx::red_release_gpu_add(&a.tile_ready[U.tile], 1u);
             }
         }
     }
