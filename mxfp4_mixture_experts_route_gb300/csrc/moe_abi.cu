@@ -121,8 +121,11 @@ static int run_route(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaS
     return cuda_rc(launch_route(s, L, p, st));
 }
 
-static int run_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
-    int rc = cuda_rc(launch_sort_gather(s, L, p, st));
+// first: the sort + gather is the call's first kernel (moe_experts), so it
+// reads x only after its wait, whatever the caller's previous kernel does;
+// after the top-k kernel (moe_forward) x is final before it may start
+static int run_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st, bool first) {
+    int rc = cuda_rc(launch_sort_gather(s, L, p, st, first));
     if (rc) return rc;
     rc = cuda_rc(launch_experts(s, L, p, st));
     if (rc) return rc;
@@ -148,7 +151,7 @@ int check_forward_args(const moe_shape* s, const void* x, const void* w_gate, co
 static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
     if (!topk_sort_fits(s)) {
         const int rc = run_route(s, L, p, st);
-        return rc ? rc : run_experts(s, L, p, st);
+        return rc ? rc : run_experts(s, L, p, st, false);
     }
     int rc = cuda_rc(launch_router_logits(s, L, p, st));
     if (!rc) rc = cuda_rc(launch_topk_sort_gather(s, L, p, st));
@@ -257,7 +260,7 @@ int moe_experts(const moe_shape* shape, const void* x, const int32_t* ids, const
     p.norm_w = (shape->flags & MOE_POST_NORM) ? norm_w : nullptr;
     p.out = out;
     p.ws = (char*)ws;
-    return run_experts(*shape, L, p, (cudaStream_t)stream);
+    return run_experts(*shape, L, p, (cudaStream_t)stream, true);
 }
 
 int moe_forward(const moe_shape* shape, const void* x, const void* w_gate, const float* bias,
@@ -478,7 +481,7 @@ int moe_latent_forward(const moe_latent_shape* shape, const void* x, const void*
             rc = cuda_rc(launch_topk_sort_gather(LL.sx, LL.Lx, px, st, true));
         } else {
             rc = cuda_rc(launch_topk(LL.sx, LL.Lx, px, st));
-            if (!rc) rc = cuda_rc(launch_sort_gather(LL.sx, LL.Lx, px, st));
+            if (!rc) rc = cuda_rc(launch_sort_gather(LL.sx, LL.Lx, px, st, true));
         }
     }
     if (!rc) rc = cuda_rc(launch_experts(LL.sx, LL.Lx, px, st));

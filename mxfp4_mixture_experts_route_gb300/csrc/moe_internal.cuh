@@ -226,7 +226,9 @@ bool route_gather_selects(const moe_shape& s);
 // call, not an input of it)
 cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st,
                                     bool x_after_wait = false);
-cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
+// the ids given (moe_experts, or the top-k kernel's); x_after_wait as above
+cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st,
+                               bool x_after_wait = false);
 cudaError_t launch_experts(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st);
 // the latent-MoE layer's elementwise steps (latent.cu)

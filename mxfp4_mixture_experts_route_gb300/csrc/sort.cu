@@ -45,12 +45,12 @@ constexpr int SMALL_SORT_PICKS = 128;   // up to this many picks, moe_experts pl
 // come from the top-k kernel (more tokens than each CTA should select again)
 // or from moe_experts' caller (up to 128 picks): every CTA reads them, checks
 // them (an id out of range or repeated by an earlier pick of its token is left
-// out, latching MOE_ERR_BAD_IDS), and only places and gathers.  As the first
-// kernel of moe_experts it reads x before its wait like every gather: the
-// caller's kernel that wrote x has completed before it may start, and none of
-// the library's kernels writes x.  The rows are
-// quantised before the wait when they are an input of the call, after it
-// when an earlier kernel of the call wrote them (x_after_wait).
+// out, latching MOE_ERR_BAD_IDS), and only places and gathers.  The rows are
+// quantised before the wait when every kernel that could write them has
+// completed before this one may start (after the router, which lets its
+// successors start only past its own wait), after it otherwise
+// (x_after_wait: rows an earlier kernel of the call wrote, or the first
+// kernel of moe_experts, whose predecessor is the caller's).
 constexpr int RG_THREADS = 512;        // at most; 16 warps: two tokens a warp at S = 32
 constexpr int RG_PASSES = 4;           // chunks of 8 elements a thread, at most: d <= 16384
 constexpr int RG_TOKENS_PER_WARP = 2;
@@ -444,10 +444,14 @@ cudaError_t launch_topk_sort_gather(const moe_shape& s, const WsLayout& L, const
     return s.E <= 256 ? launch_rg<8, false>(s, L, p, st, x_after_wait) : launch_rg<16, false>(s, L, p, st, x_after_wait);
 }
 
-cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st,
+                               bool x_after_wait) {
     KT_BIND();
     const int P = s.S * s.k;
     if (P > SMALL_SORT_PICKS) {
+        // k_gather_tok reads the rows before its wait even when an earlier
+        // kernel of the call wrote them: k_count lets it start only past its
+        // own wait, when every kernel before k_count has completed
         const CountOut c = count_out(L, p.ws);
         timing_begin(K_SORT, st);
         cudaError_t e = launch_pdl(k_count, dim3((P + CNT_THREADS - 1) / CNT_THREADS), dim3(CNT_THREADS), 0, st,
@@ -464,8 +468,10 @@ cudaError_t launch_sort_gather(const moe_shape& s, const WsLayout& L, const Ptrs
         return e;
     }
     // up to 128 picks: the fused kernel reads the ids, checks them, places
-    // every pick and gathers its row in one launch
-    return launch_rg<8, true>(s, L, p, st, false);
+    // every pick and gathers its row in one launch (after its wait when an
+    // earlier kernel of the call wrote the rows: the top-k kernel before it
+    // lets it start before that kernel's own wait)
+    return launch_rg<8, true>(s, L, p, st, x_after_wait);
 }
 
 }  // namespace moe

@@ -61,6 +61,11 @@ CASES = [
     # (with the shared gate/up: three products of x in one launch; without it, two)
     mi.LatentConfig("lg_s5_router_part", S=5, H=256, LAT=256, E=128, k=4, I=128, SI=256),
     mi.LatentConfig("lg_s2_router_part_noshared", S=2, H=384, LAT=128, E=256, k=2, I=256, SI=0, zipf=1.1),
+    # more than 32 tokens: the top-k kernel, then up to 128 picks the fused
+    # sort + gather after its wait (the latent rows are the call's own), above
+    # that the counting sort and the per-token gather
+    mi.LatentConfig("lg_s40_k3", S=40, H=256, LAT=256, E=16, k=3, I=128, SI=128),
+    mi.LatentConfig("lg_s48_k4", S=48, H=256, LAT=384, E=12, k=4, I=128, SI=0),
 ]
 
 
