@@ -185,12 +185,12 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate,
 /*
  * moe_forward with the step's input and outputs in HOST memory: x_host [S, d]
  * bf16 in, ids_host [S, k], weights_host [S, k], out_host [S, d] out, all
- * enqueued on `stream`.  A small pinned buffer the GPU can address
- * (cudaHostAlloc'd or cudaHostRegister'ed memory; on GB300 over the coherent
- * CPU-GPU link), 16-byte aligned, is read or written in place by the kernels:
- * x when S <= 8, ids and weights when S <= 32 and S * k <= 1024, out when
- * S * d * 4 <= 256 KiB.  Every other host buffer (pageable, unaligned or
- * larger) is staged through the workspace with one cudaMemcpyAsync.  The weights (w_gate,
+ * enqueued on `stream`.  An output in a small pinned buffer the GPU can
+ * address (cudaHostAlloc'd or cudaHostRegister'ed memory; on GB300 over the
+ * coherent CPU-GPU link), 16-byte aligned, is written in place by the kernels:
+ * ids and weights when S <= 32 and S * k <= 128, out when S * d * 4 <= 256 KiB.
+ * x and every other host buffer (pageable, unaligned or larger) is staged
+ * through the workspace with one cudaMemcpyAsync.  The weights (w_gate,
  * bias, logit_off, w13, w13s, w2, w2s, norm_w) stay device pointers.  The host
  * buffers must not be touched until the stream has been synchronised.
  * ids_host / weights_host may be NULL (then only out is returned).

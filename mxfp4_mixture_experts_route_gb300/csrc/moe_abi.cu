@@ -358,19 +358,18 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     rc = check_ws(shape, ws, ws_bytes);
     if (!rc) rc = check_device();
     if (rc) return rc;
-    // A small pinned host buffer is read or written in place by the kernels
-    // (measured faster than a copy): x when the router reads all of it in one
-    // round of loads (S <= 8), ids and weights when the fused top-k + sort +
-    // gather writes them (one CTA a pick), out up to 256 KB.  Every other
-    // buffer goes through the workspace's host-I/O staging regions (xin,
-    // hio_ids, hio_w, hio_out) and one copy, which moves bulk data faster than
-    // the kernels' own loads and stores over the link.
+    // A small pinned host buffer the kernels write is written in place
+    // (measured faster than a copy at S = 8: 7 to 8 us a step for each of out
+    // and ids + weights): ids and weights when the fused top-k + sort + gather
+    // writes them (one CTA a pick), out up to 256 KB.  x, which the router and
+    // the gather both read, and every other buffer go through the workspace's
+    // host-I/O staging regions (xin, hio_ids, hio_w, hio_out) and one copy
+    // (x in place cost 2.7 us a step at S = 8).
     WsLayout L = ws_layout(*shape);
     cudaStream_t st = (cudaStream_t)stream;
     char* w = (char*)ws;
     const size_t P = (size_t)shape->S * shape->k;
     const bool small_out = (size_t)shape->S * shape->d * 4 <= (256u << 10);
-    void* x_dev = shape->S <= 8 ? device_view(x_host) : nullptr;
     int32_t* ids_dev = ids_host && route_gather_selects(*shape) ? (int32_t*)device_view(ids_host) : nullptr;
     float* wts_dev = weights_host && route_gather_selects(*shape) ? (float*)device_view(weights_host) : nullptr;
     float* out_dev = small_out ? (float*)device_view(out_host) : nullptr;
@@ -378,11 +377,9 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     if (!ids_dev) ids_dev = (int32_t*)(w + L.hio_ids);
     if (!wts_dev) wts_dev = (float*)(w + L.hio_w);
     if (!out_dev) out_dev = (float*)(w + L.hio_out);
-    if (!x_dev) {
-        x_dev = w + L.xin;
-        rc = cuda_rc(cudaMemcpyAsync(x_dev, x_host, (size_t)shape->S * shape->d * 2, cudaMemcpyHostToDevice, st));
-        if (rc) return rc;
-    }
+    void* x_dev = w + L.xin;
+    rc = cuda_rc(cudaMemcpyAsync(x_dev, x_host, (size_t)shape->S * shape->d * 2, cudaMemcpyHostToDevice, st));
+    if (rc) return rc;
     rc = moe_forward(shape, x_dev, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids_dev, wts_dev,
                      out_dev, ws, ws_bytes, stream);
     if (rc) return rc;
