@@ -189,8 +189,10 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate,
  * address (cudaHostAlloc'd or cudaHostRegister'ed memory; on GB300 over the
  * coherent CPU-GPU link), 16-byte aligned, is written in place by the kernels:
  * ids and weights when S <= 32 and S * k <= 128, out when S * d * 4 <= 256 KiB.
- * x and every other host buffer (pageable, unaligned or larger) is staged
- * through the workspace with one cudaMemcpyAsync.  The weights (w_gate,
+ * x is copied into the workspace, from a pinned buffer up to 1 MiB by a kernel
+ * (which lets the router start meanwhile), else with one cudaMemcpyAsync; every
+ * other host buffer (pageable, unaligned or larger) is staged through the
+ * workspace with one cudaMemcpyAsync.  The weights (w_gate,
  * bias, logit_off, w13, w13s, w2, w2s, norm_w) stay device pointers.  The host
  * buffers must not be touched until the stream has been synchronised.
  * ids_host / weights_host may be NULL (then only out is returned).

@@ -160,6 +160,10 @@ static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cud
     return rc;
 }
 
+// x from pinned host memory into the workspace by a kernel (hostio.cu):
+// bytes a multiple of 16, both addresses 16-byte aligned
+cudaError_t launch_stage_in(const void* src, void* dst, size_t bytes, cudaStream_t st);
+
 }  // namespace moe
 
 using namespace moe;
@@ -377,8 +381,13 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     if (!ids_dev) ids_dev = (int32_t*)(w + L.hio_ids);
     if (!wts_dev) wts_dev = (float*)(w + L.hio_w);
     if (!out_dev) out_dev = (float*)(w + L.hio_out);
+    // x by a kernel from a pinned buffer up to 1 MB (the router starts while
+    // it runs), by the copy engine otherwise
     void* x_dev = w + L.xin;
-    rc = cuda_rc(cudaMemcpyAsync(x_dev, x_host, (size_t)shape->S * shape->d * 2, cudaMemcpyHostToDevice, st));
+    const size_t x_bytes = (size_t)shape->S * shape->d * 2;
+    const void* x_view = x_bytes <= (1u << 20) ? device_view(x_host) : nullptr;
+    rc = cuda_rc(x_view ? launch_stage_in(x_view, x_dev, x_bytes, st)
+                        : cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st));
     if (rc) return rc;
     rc = moe_forward(shape, x_dev, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids_dev, wts_dev,
                      out_dev, ws, ws_bytes, stream);
