@@ -22,9 +22,14 @@ constexpr int CB_MAXK = 16;               // picks per token (k <= 16)
 // writes: warp w adds up the blocks of picks w and w + 8 (lanes over blocks,
 // then a fixed shuffle tree), so the CTA never reads a whole y row twice.
 // y rows are addressed through pos[t*k + j] (the sorted per-pick buffer).
+// ids_out / w_out (host buffers of moe_forward_host, or null): the CTAs of
+// column block 0 also copy the token's ids and routing weights there from
+// the workspace, so that those writes over the CPU-GPU link go out with the
+// block's last kernel instead of holding up the routing kernel's completion.
 __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const float* ssq, const int32_t* pos, const float* w,
                                                         const float* __restrict__ norm_w, float eps, int k, int d,
-                                                        float* __restrict__ out) {
+                                                        float* __restrict__ out, const int32_t* ids,
+                                                        int32_t* __restrict__ ids_out, float* __restrict__ w_out) {
     KT_MARK(K_COMBINE, 0);
     pdl_trigger();
     pdl_wait();
@@ -39,6 +44,10 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const fl
         if (j < k) {
             const int p = ld_dep(pos + (size_t)t * k + j);
             float c = ld_dep(w + (size_t)t * k + j);
+            if (ids_out != nullptr && blockIdx.y == 0 && lane == 0) {
+                ids_out[(size_t)t * k + j] = ld_dep(ids + (size_t)t * k + j);
+                w_out[(size_t)t * k + j] = c;
+            }
             if (norm_w != nullptr && p >= 0) {
                 const int nb = d / 128;                // <= 128 row blocks
                 float q = 0.f;
@@ -93,16 +102,23 @@ __global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const fl
 
 }  // namespace
 
-cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+// ids_out / w_out: see k_combine (both null: the plain combine)
+cudaError_t launch_combine_host(const moe_shape& s, const WsLayout& L, const Ptrs& p, int32_t* ids_out, float* w_out,
+                                cudaStream_t st) {
     KT_BIND();
     timing_begin(K_COMBINE, st);
     const dim3 grid(s.S, (s.d + CB_COLS - 1) / CB_COLS);
     const cudaError_t e =
         launch_pdl(k_combine, grid, dim3(CB_THREADS), 0, st, reinterpret_cast<const float*>(p.ws + L.y),
                    reinterpret_cast<const float*>(p.ws + L.ssq), reinterpret_cast<const int32_t*>(p.ws + L.pos),
-                   (const float*)p.weights, p.norm_w, s.norm_eps, s.k, s.d, p.out);
+                   (const float*)p.weights, p.norm_w, s.norm_eps, s.k, s.d, p.out, (const int32_t*)p.ids, ids_out,
+                   w_out);
     timing_end(st);
     return e;
+}
+
+cudaError_t launch_combine(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+    return launch_combine_host(s, L, p, nullptr, nullptr, st);
 }
 
 }  // namespace moe

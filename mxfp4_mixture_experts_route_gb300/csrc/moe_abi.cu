@@ -7,6 +7,13 @@
 
 namespace moe {
 
+// x from pinned host memory into the workspace by a kernel (hostio.cu):
+// bytes a multiple of 16, both addresses 16-byte aligned
+cudaError_t launch_stage_in(const void* src, void* dst, size_t bytes, cudaStream_t st);
+// the combine that also copies ids and weights to host buffers (combine.cu)
+cudaError_t launch_combine_host(const moe_shape& s, const WsLayout& L, const Ptrs& p, int32_t* ids_out, float* w_out,
+                                cudaStream_t st);
+
 static size_t align256(size_t v) { return (v + 255) & ~size_t(255); }
 
 // Picks per expert tile: 8 while the average expert gets at most 2 picks (the
@@ -148,7 +155,10 @@ int check_forward_args(const moe_shape* s, const void* x, const void* w_gate, co
 
 // The whole block.  At small S the top-k, the sort and the gather share one
 // kernel (two launches and two kernel boundaries fewer).
-static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st) {
+// ids_out / w_out (moe_forward_host at small S, or null): host buffers the
+// combine copies the ids and weights to.
+static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st,
+                       int32_t* ids_out = nullptr, float* w_out = nullptr) {
     if (!topk_sort_fits(s)) {
         const int rc = run_route(s, L, p, st);
         return rc ? rc : run_experts(s, L, p, st, false);
@@ -156,13 +166,36 @@ static int run_forward(const moe_shape& s, const WsLayout& L, const Ptrs& p, cud
     int rc = cuda_rc(launch_router_logits(s, L, p, st));
     if (!rc) rc = cuda_rc(launch_topk_sort_gather(s, L, p, st));
     if (!rc) rc = cuda_rc(launch_experts(s, L, p, st));
-    if (!rc) rc = cuda_rc(launch_combine(s, L, p, st));
+    if (!rc) rc = cuda_rc(launch_combine_host(s, L, p, ids_out, w_out, st));
     return rc;
 }
 
-// x from pinned host memory into the workspace by a kernel (hostio.cu):
-// bytes a multiple of 16, both addresses 16-byte aligned
-cudaError_t launch_stage_in(const void* src, void* dst, size_t bytes, cudaStream_t st);
+// moe_forward; ids_out / w_out (host buffers, or null): the combine also
+// copies the ids and weights there (moe_forward_host at small S)
+static int forward_impl(const moe_shape* shape, const void* x, const void* w_gate, const float* bias,
+                        const float* logit_off, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
+                        const uint8_t* w2s, const float* norm_w, int32_t* ids, float* weights, float* out,
+                        void* ws, size_t ws_bytes, void* stream, int32_t* ids_out, float* w_out) {
+    int rc = check_shape(shape);
+    if (!rc) rc = check_route_args(shape, x, w_gate, bias, logit_off, ids, weights);
+    if (!rc) rc = check_expert_args(shape, x, ids, weights, w13, w13s, w2, w2s, norm_w, out);
+    if (!rc) rc = check_ws(shape, ws, ws_bytes);
+    if (!rc) rc = check_device();
+    if (rc) return rc;
+    WsLayout L = ws_layout(*shape);
+    Ptrs p{};
+    p.x = (const __nv_bfloat16*)x;
+    p.w_gate = (const __nv_bfloat16*)w_gate;
+    p.bias = bias;
+    p.logit_off = (shape->flags & MOE_LOGIT_OFFSET) ? logit_off : nullptr;
+    p.w13 = w13; p.w13s = w13s; p.w2 = w2; p.w2s = w2s;
+    p.norm_w = (shape->flags & MOE_POST_NORM) ? norm_w : nullptr;
+    p.ids = ids;
+    p.weights = weights;
+    p.out = out;
+    p.ws = (char*)ws;
+    return run_forward(*shape, L, p, (cudaStream_t)stream, ids_out, w_out);
+}
 
 }  // namespace moe
 
@@ -271,25 +304,8 @@ int moe_forward(const moe_shape* shape, const void* x, const void* w_gate, const
                 const float* logit_off, const uint8_t* w13, const uint8_t* w13s, const uint8_t* w2,
                 const uint8_t* w2s, const float* norm_w, int32_t* ids, float* weights, float* out,
                 void* ws, size_t ws_bytes, void* stream) {
-    int rc = check_shape(shape);
-    if (!rc) rc = check_route_args(shape, x, w_gate, bias, logit_off, ids, weights);
-    if (!rc) rc = check_expert_args(shape, x, ids, weights, w13, w13s, w2, w2s, norm_w, out);
-    if (!rc) rc = check_ws(shape, ws, ws_bytes);
-    if (!rc) rc = check_device();
-    if (rc) return rc;
-    WsLayout L = ws_layout(*shape);
-    Ptrs p{};
-    p.x = (const __nv_bfloat16*)x;
-    p.w_gate = (const __nv_bfloat16*)w_gate;
-    p.bias = bias;
-    p.logit_off = (shape->flags & MOE_LOGIT_OFFSET) ? logit_off : nullptr;
-    p.w13 = w13; p.w13s = w13s; p.w2 = w2; p.w2s = w2s;
-    p.norm_w = (shape->flags & MOE_POST_NORM) ? norm_w : nullptr;
-    p.ids = ids;
-    p.weights = weights;
-    p.out = out;
-    p.ws = (char*)ws;
-    return run_forward(*shape, L, p, (cudaStream_t)stream);
+    return forward_impl(shape, x, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids, weights, out, ws, ws_bytes,
+                        stream, nullptr, nullptr);
 }
 
 }  // extern "C"
@@ -362,24 +378,27 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     rc = check_ws(shape, ws, ws_bytes);
     if (!rc) rc = check_device();
     if (rc) return rc;
-    // A small pinned host buffer the kernels write is written in place
-    // (measured faster than a copy at S = 8: 7 to 8 us a step for each of out
-    // and ids + weights): ids and weights when the fused top-k + sort + gather
-    // writes them (one CTA a pick), out up to 256 KB.  x, which the router and
+    // A small pinned host buffer for an output is written over the link by a
+    // kernel (measured faster than a copy afterwards at S = 8: 7 to 8 us a step
+    // for each of out and ids + weights): out up to 256 KB by the combine, and
+    // ids and weights, when the fused top-k + sort + gather produces them,
+    // copied from the workspace by the combine too (so that those writes do
+    // not hold up the routing kernel's completion).  x, which the router and
     // the gather both read, and every other buffer go through the workspace's
-    // host-I/O staging regions (xin, hio_ids, hio_w, hio_out) and one copy
-    // (x in place cost 2.7 us a step at S = 8).
+    // host-I/O staging regions (xin, hio_ids, hio_w, hio_out).
     WsLayout L = ws_layout(*shape);
     cudaStream_t st = (cudaStream_t)stream;
     char* w = (char*)ws;
     const size_t P = (size_t)shape->S * shape->k;
     const bool small_out = (size_t)shape->S * shape->d * 4 <= (256u << 10);
-    int32_t* ids_dev = ids_host && route_gather_selects(*shape) ? (int32_t*)device_view(ids_host) : nullptr;
-    float* wts_dev = weights_host && route_gather_selects(*shape) ? (float*)device_view(weights_host) : nullptr;
+    // ids and weights go to the workspace; the combine copies them to pinned
+    // host buffers at small S, a copy afterwards does otherwise
+    int32_t* ids_view = ids_host && route_gather_selects(*shape) ? (int32_t*)device_view(ids_host) : nullptr;
+    float* wts_view = weights_host && route_gather_selects(*shape) ? (float*)device_view(weights_host) : nullptr;
     float* out_dev = small_out ? (float*)device_view(out_host) : nullptr;
-    const bool ids_staged = !ids_dev, wts_staged = !wts_dev, out_staged = !out_dev;
-    if (!ids_dev) ids_dev = (int32_t*)(w + L.hio_ids);
-    if (!wts_dev) wts_dev = (float*)(w + L.hio_w);
+    const bool ids_staged = !ids_view, wts_staged = !wts_view, out_staged = !out_dev;
+    int32_t* ids_dev = (int32_t*)(w + L.hio_ids);
+    float* wts_dev = (float*)(w + L.hio_w);
     if (!out_dev) out_dev = (float*)(w + L.hio_out);
     // x by a kernel from a pinned buffer up to 1 MB (the router starts while
     // it runs), by the copy engine otherwise
@@ -389,8 +408,8 @@ int moe_forward_host(const moe_shape* shape, const void* x_host, const void* w_g
     rc = cuda_rc(x_view ? launch_stage_in(x_view, x_dev, x_bytes, st)
                         : cudaMemcpyAsync(x_dev, x_host, x_bytes, cudaMemcpyHostToDevice, st));
     if (rc) return rc;
-    rc = moe_forward(shape, x_dev, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids_dev, wts_dev,
-                     out_dev, ws, ws_bytes, stream);
+    rc = forward_impl(shape, x_dev, w_gate, bias, logit_off, w13, w13s, w2, w2s, norm_w, ids_dev, wts_dev, out_dev,
+                      ws, ws_bytes, stream, ids_view, wts_view);
     if (rc) return rc;
     if (out_staged)
         rc = cuda_rc(cudaMemcpyAsync(out_host, out_dev, (size_t)shape->S * shape->d * 4, cudaMemcpyDeviceToHost, st));
