@@ -346,9 +346,10 @@ def test_scale_range(shift13, shift2):
 
 @pytest.mark.parametrize("ci,pinned", [(1, True), (1, False), (2, True), (3, True)])
 def test_forward_host_matches_forward(ci, pinned):
-    """Host buffers: small pinned ones are read and written in place by the
-    kernels (all four at S = 8, ids and weights at S = 32), the others are
-    staged through the workspace; either way the bytes equal moe_forward's."""
+    """Host buffers: a small pinned x is copied in by the staging kernel (S = 8
+    and 32), small pinned outputs are written over the link by the combine
+    (out, ids and weights at S = 8), the others go through the workspace and a
+    copy (pageable ones, S = 128's x); either way the bytes equal moe_forward's."""
     import torch
     inp = mi.make_inputs(mi.CONFIGS[ci])
     blk = device_block(inp)
