@@ -42,3 +42,12 @@ def test_algorithmic_bytes_per_expert():
     alg = bench.algorithmic_bytes(cfg, 1)
     assert alg["experts"] == 3 * cfg.I * cfg.d * 17 // 32 == 3342336
     assert alg["step"] == alg["experts"] + cfg.E * cfg.d * 2 + 4 * cfg.E
+
+
+def test_ktrace_cli_parses():
+    """The trace-timeline tool's command line (the tool itself needs a GPU)."""
+    import pytest
+    from mxfp4_mixture_experts_route_gb300 import ktrace
+    with pytest.raises(SystemExit) as e:
+        ktrace.main(["--help"])
+    assert e.value.code == 0
