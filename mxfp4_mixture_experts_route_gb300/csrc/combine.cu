@@ -26,7 +26,12 @@ constexpr int CB_MAXK = 16;               // picks per token (k <= 16)
 // column block 0 also copy the token's ids and routing weights there from
 // the workspace, so that those writes over the CPU-GPU link go out with the
 // block's last kernel instead of holding up the routing kernel's completion.
-__global__ void __launch_bounds__(CB_THREADS) k_combine(const float* y, const float* ssq, const int32_t* pos, const float* w,
+// At most 32 registers a thread (eight CTAs an SM's worth): a combine CTA
+// starts beside an expert CTA (programmatic dependent launch) only if it fits
+// in what that CTA leaves of each SM sub-partition's register file, 2048
+// registers where four of the expert CTA's warps sit (4 x 32 x 112 of 16384),
+// i.e. two warps of 32 registers a thread.
+__global__ void __launch_bounds__(CB_THREADS, 8) k_combine(const float* y, const float* ssq, const int32_t* pos, const float* w,
                                                         const float* __restrict__ norm_w, float eps, int k, int d,
                                                         float* __restrict__ out, const int32_t* ids,
                                                         int32_t* __restrict__ ids_out, float* __restrict__ w_out) {
