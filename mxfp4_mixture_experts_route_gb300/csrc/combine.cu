@@ -22,8 +22,8 @@ constexpr int CB_MAXK = 16;               // picks per token (k <= 16)
 // writes: warp w adds up the blocks of picks w and w + 8 (lanes over blocks,
 // then a fixed shuffle tree), so the CTA never reads a whole y row twice.
 // y rows are addressed through pos[t*k + j] (the sorted per-pick buffer).
-// ids_out / w_out (host buffers of moe_forward_host, or null): the CTAs of
-// column block 0 also copy the token's ids and routing weights there from
+// ids_out / w_out (host buffers of moe_forward_host, each or both null): the
+// CTAs of column block 0 also copy the token's ids and routing weights there from
 // the workspace, so that those writes over the CPU-GPU link go out with the
 // block's last kernel instead of holding up the routing kernel's completion.
 // At most 32 registers a thread (eight CTAs an SM's worth): a combine CTA
@@ -49,9 +49,9 @@ __global__ void __launch_bounds__(CB_THREADS, 8) k_combine(const float* y, const
         if (j < k) {
             const int p = ld_dep(pos + (size_t)t * k + j);
             float c = ld_dep(w + (size_t)t * k + j);
-            if (ids_out != nullptr && blockIdx.y == 0 && lane == 0) {
-                ids_out[(size_t)t * k + j] = ld_dep(ids + (size_t)t * k + j);
-                w_out[(size_t)t * k + j] = c;
+            if (blockIdx.y == 0 && lane == 0) {   // either may be null
+                if (ids_out != nullptr) ids_out[(size_t)t * k + j] = ld_dep(ids + (size_t)t * k + j);
+                if (w_out != nullptr) w_out[(size_t)t * k + j] = c;
             }
             if (norm_w != nullptr && p >= 0) {
                 const int nb = d / 128;                // <= 128 row blocks

@@ -371,6 +371,30 @@ def test_forward_host_matches_forward(ci, pinned):
     assert np.array_equal(oh.numpy(), out)
 
 
+@pytest.mark.parametrize("want", ["ids", "weights", "neither"])
+def test_forward_host_one_routing_output(want):
+    """ids_host and weights_host may each be NULL: the other (pinned, written
+    by the combine at S = 8) and out still come back."""
+    import torch
+    inp = mi.make_inputs(mi.CONFIGS[1])
+    blk = device_block(inp)
+    ids, w, out = [t.cpu().numpy() for t in blk.forward()]
+    s = blk.shape
+    xh = torch.as_tensor(inp.x).view(torch.bfloat16).clone().pin_memory()
+    oh = torch.empty((s.S, s.d), dtype=torch.float32).pin_memory()
+    ih = torch.full((s.S, s.k), -7, dtype=torch.int32).pin_memory() if want == "ids" else None
+    wh = torch.full((s.S, s.k), -7.0, dtype=torch.float32).pin_memory() if want == "weights" else None
+    moe.forward_host(s, xh, blk.w_gate, blk.bias, blk.logit_off, blk.w13, blk.w13s, blk.w2, blk.w2s,
+                     blk.norm_w, ih, wh, oh, blk.ws)
+    torch.cuda.current_stream().synchronize()
+    moe.check_device_status(blk.ws)
+    assert np.array_equal(oh.numpy(), out)
+    if ih is not None:
+        assert np.array_equal(ih.numpy(), ids)
+    if wh is not None:
+        assert np.array_equal(wh.numpy(), w)
+
+
 @pytest.mark.parametrize("ci", [2, 3])
 def test_repeat_calls_are_deterministic(ci):
     """Synchronised calls with other work on the stream in between (a write
