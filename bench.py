@@ -475,22 +475,22 @@ def run_ours(args, cfg: mi.MoEConfig):
     flush = L2Flush(dev, l2)
     stream = torch.cuda.current_stream(dev)
 
-    for _ in range(args.warmup):
-        flush.zero_()
-        blk.forward()
-    moe.check_device_status(blk.ws, "warmup")
-    ids = blk.ids.cpu().numpy()
-    n_touched = int(len(np.unique(ids)))
-
     # --- timed region -------------------------------------------------------
+    # the clock sampler starts first (nvidia-smi takes a moment to come up);
+    # the W warm-up steps then run right before the timed ones, so that the
+    # first timed step finds the host path as warm as the others (after an
+    # idle host gap the first step's enqueue no longer hides behind the flush)
     K = args.steps
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(K)]
     clocks = ClockSampler(local)
+    clocks.start()
+    time.sleep(0.3)
+    for _ in range(args.warmup):
+        flush.zero_()
+        blk.forward()
     torch.cuda.synchronize(dev)
     if dist:
         dist.barrier()
-    clocks.start()
-    time.sleep(0.05)
     wall0 = time.perf_counter()
     for i in range(K):
         flush.zero_()
@@ -504,6 +504,8 @@ def run_ours(args, cfg: mi.MoEConfig):
     clk = clocks.stop()
     step_ms = [a.elapsed_time(b) for a, b in ev]
     moe.check_device_status(blk.ws, "timed steps")
+    ids = blk.ids.cpu().numpy()
+    n_touched = int(len(np.unique(ids)))
     ms_total, units = aggregate(dist, sum(step_ms), K * cfg.S, dev)
     value = units / (ms_total / 1e3)
 
