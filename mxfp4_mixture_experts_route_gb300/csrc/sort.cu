@@ -54,6 +54,7 @@ constexpr int SMALL_SORT_PICKS = 128;   // up to this many picks, moe_experts pl
 constexpr int RG_THREADS = 512;        // at most; 16 warps: two tokens a warp at S = 32
 constexpr int RG_PASSES = 4;           // chunks of 8 elements a thread, at most: d <= 16384
 constexpr int RG_TOKENS_PER_WARP = 2;
+constexpr size_t RG_ONE_PER_SM_SMEM = 117 * 1024;   // over half an SM's 228 KB
 template <int MAXE, int PASSES, bool FROM_IDS>
 __global__ void __launch_bounds__(RG_THREADS) k_route_gather(const float* L, const float* __restrict__ bias,
                                                             const __nv_bfloat16* __restrict__ x, int S, int E,
@@ -415,9 +416,14 @@ template <int MAXE, bool FROM_IDS>
 static cudaError_t launch_rg(const moe_shape& s, const WsLayout& L, const Ptrs& p, cudaStream_t st, bool x_after_wait) {
     const int threads = route_gather_threads(s);
     const int P = s.S * s.k;
-    const size_t smem = (size_t)(P + s.E) * sizeof(int32_t) +
-                        (FROM_IDS ? (size_t)P * sizeof(int32_t)
-                                  : (size_t)std::min(s.S, threads / 32) * 32 * MAXE * sizeof(float));
+    size_t smem = (size_t)(P + s.E) * sizeof(int32_t) +
+                  (FROM_IDS ? (size_t)P * sizeof(int32_t)
+                            : (size_t)std::min(s.S, threads / 32) * 32 * MAXE * sizeof(float));
+    // one CTA an SM when the picks fit one wave: two CTAs on an SM finished
+    // their selection up to 1.3 us apart, and the slowest CTA decides when the
+    // expert kernel's wait returns (S = 8: the step 52.3 against 53.0 us).  The
+    // shared memory asked for is what makes a second CTA not fit.
+    if (P <= num_sms() && smem < RG_ONE_PER_SM_SMEM) smem = RG_ONE_PER_SM_SMEM;
     const int passes = (s.d / 8 + threads - 1) / threads;   // 1, 2 or 4 (d <= 16384)
     auto kern = passes == 1 ? k_route_gather<MAXE, 1, FROM_IDS>
                             : passes == 2 ? k_route_gather<MAXE, 2, FROM_IDS> : k_route_gather<MAXE, 4, FROM_IDS>;
